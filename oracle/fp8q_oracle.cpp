@@ -1,0 +1,353 @@
+// fp8q oracle -- TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, single-threaded C++ restatement of what the FP8 transfer
+// codec computes.  Only the test suite, the smoke check and the CPU-baseline
+// leg of the benchmark may load this file's library; the product path
+// (the CUDA library under weight_transfer_gb300/) never does, and the two
+// share no code, header, table or constant.
+//
+// Build: g++ -O2 -ffp-contract=off -fPIC -shared (no -ffast-math, no FMA
+// contraction, no flush-to-zero), so every float expression below is one
+// IEEE-754 binary32 operation rounded to nearest-even.
+//
+// Sources (web pages; quoted by title and section):
+//  [P1] "FP8 Transmission Optimization for VLA Training: Byte Reduction Leads
+//       to Increased Latency", intro and section "FP8 Transmission
+//       Optimization and Bottlenecks": blockwise-scaled e4m3/e5m2 wire format,
+//       fused dequantize-then-reduce, ring collectives.
+//  [P2] "How to Speed Up VLA Training Step by Step: 3x on Pi0.5", paragraph
+//       on PCIe gradient communication: ring AllReduce of bf16 gradients.
+//  [P3] "perf: Reduce MXFP8 refit weight-transfer overheads" (NeMo-RL PR
+//       #3294), Summary, Safety, self-review ("E8M0 zero-scale clamp",
+//       "2D/3D reshape") and the inline review on the K == 32 scale squeeze.
+//  [OFP8] OCP 8-bit Floating Point Specification (OFP8), rev. 1.0: bit
+//       layouts of E4M3 (bias 7, no infinities, S.1111.111 = NaN) and E5M2
+//       (bias 15, IEEE-like infinities and NaNs).
+//  [MX] OCP Microscaling Formats (MX) Specification v1.0: E8M0 shared scale,
+//       X = floor(log2(amax)) - emax_elem.
+//
+// The pages print no formula or code for any of these steps.  The readings
+// taken where they are silent are (numbered as in the design notes):
+//  O1 block of 128 elements with one fp32 scale (the only reading that gives
+//     P1's 48.4% byte saving exactly);
+//  O2/O3 s = RN(amax / Fmax); code = RNE_fp8(RN_fp32(x / s)), a true IEEE
+//     division followed by the format's own rounding;
+//  O4 all-zero block: s = 0 and each code is the signed zero of x;
+//  O5 saturate to the largest finite code, never produce inf/NaN from
+//     finite input;
+//  O7 the last block may be partial: its amax covers the valid elements;
+//  O8 the reduce is a sum in rank order 0..k-1 starting from +0, each
+//     product and each add rounded separately;
+//  O9 the ring hop requantizes the fp32 sum, not its bf16 rounding;
+//  O11/O12 E8M0 e = clamp(floor(log2 amax) - 8 + 127, 0, 254), amax == 0
+//     gives e = 0;
+//  O14 scale swizzle: 128x4 tiles of 512 bytes,
+//     (r%32)*16 + ((r%128)/32)*4 + (j%4) inside a tile.
+//  O17 K % 32 != 0 is rejected; K == 32 keeps its one real scale column.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+namespace {
+
+// ---------------------------------------------------------------- formats --
+// [OFP8] section 4: E4M3 = 1 sign, 4 exponent (bias 7), 3 mantissa bits,
+// S.1111.111 is NaN and there is no infinity, largest finite 0x7E = 448.
+// E5M2 = 1 sign, 5 exponent (bias 15), 2 mantissa bits; exponent 31 holds
+// infinities (mantissa 0) and NaNs, largest finite 0x7B = 57344.
+struct Fmt {
+    int ebits, mbits, bias;
+    uint8_t max_code;   // largest finite magnitude code
+    float max_value;    // its value
+};
+
+const Fmt kE4M3 = {4, 3, 7, 0x7E, 448.0f};
+const Fmt kE5M2 = {5, 2, 15, 0x7B, 57344.0f};
+
+const Fmt& fmt_of(int fmt) { return fmt == 1 ? kE5M2 : kE4M3; }
+
+uint32_t f32_bits(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
+float bits_f32(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
+
+// Value of one code, straight from the field definitions.
+double decode_exact(const Fmt& F, uint8_t c) {
+    int s = c >> 7;
+    int E = (c >> F.mbits) & ((1 << F.ebits) - 1);
+    int M = c & ((1 << F.mbits) - 1);
+    int Emax = (1 << F.ebits) - 1;
+    double sign = s ? -1.0 : 1.0;
+    if (F.ebits == 4 && E == Emax && M == (1 << F.mbits) - 1) return NAN;   // E4M3 NaN
+    if (F.ebits == 5 && E == Emax) return M == 0 ? sign * INFINITY : NAN;    // E5M2 inf/NaN
+    if (E == 0) return sign * std::ldexp((double)M, 1 - F.bias - F.mbits);  // subnormal
+    return sign * std::ldexp((double)((1 << F.mbits) + M), E - F.bias - F.mbits);
+}
+
+bool is_nan_code(const Fmt& F, uint8_t c) { return std::isnan(decode_exact(F, c)); }
+bool is_inf_code(const Fmt& F, uint8_t c) { return std::isinf(decode_exact(F, c)); }
+
+// Round-to-nearest-even of the binary32 value v to the FP8 format, then
+// saturate to +-max finite ([OFP8] "satfinite" conversion; reading O5).
+// Works on the integer significand of v so no floating-point rounding mode
+// is involved.
+uint8_t encode_bits(const Fmt& F, float v) {
+    uint32_t u = f32_bits(v);
+    uint8_t sign = (uint8_t)((u >> 31) << 7);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return (uint8_t)(sign | 0x7F);              // NaN -> a NaN code
+    if (bits_f32(a) > F.max_value) return (uint8_t)(sign | F.max_code);  // incl. inf
+    if (a == 0) return sign;                                          // signed zero
+    // v = sig * 2^exp2 exactly, sig < 2^24.
+    uint32_t E32 = a >> 23, M32 = a & 0x7FFFFFu;
+    uint32_t sig = E32 ? (M32 | 0x800000u) : M32;
+    int exp2 = E32 ? (int)E32 - 150 : -149;
+    int bitlen = 32 - __builtin_clz(sig);
+    int e = exp2 + bitlen - 1;                 // floor(log2 |v|)
+    int emin = 1 - F.bias;                     // exponent of the smallest normal
+    int qexp = (e < emin ? emin : e) - F.mbits;   // exponent of one ulp of the result
+    int shift = qexp - exp2;                   // >= 0 for both formats
+    uint64_t q;                                // |v| / 2^qexp rounded to nearest even
+    if (shift >= 40) {
+        q = 0;                                 // far below half an ulp
+    } else {
+        uint64_t s64 = sig;
+        q = s64 >> shift;
+        uint64_t rem = s64 - (q << shift);
+        uint64_t half = shift ? (1ull << (shift - 1)) : 0;
+        if (shift && (rem > half || (rem == half && (q & 1)))) q += 1;
+    }
+    uint32_t code;
+    if (e < emin) {
+        code = (uint32_t)q;                    // subnormal; q == 2^m is the smallest normal
+    } else {
+        int ee = e;
+        if (q == (2ull << F.mbits)) { ee += 1; q = 1ull << F.mbits; }   // carried into exponent
+        code = ((uint32_t)(ee + F.bias) << F.mbits) | (uint32_t)(q - (1ull << F.mbits));
+    }
+    if (code > F.max_code) code = F.max_code;  // cannot happen for |v| <= max, kept as a guard
+    return (uint8_t)(sign | code);
+}
+
+// Brute force: the finite code nearest to v, ties to the code whose last
+// mantissa bit is 0, saturated to +-max.  Independent of encode_bits().
+uint8_t encode_brute(const Fmt& F, float v) {
+    if (std::isnan(v)) return (uint8_t)((std::signbit(v) ? 0x80 : 0) | 0x7F);
+    double a = std::fabs((double)v);
+    uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+    if (a > F.max_value) return (uint8_t)(sign | F.max_code);
+    int best = -1;
+    double best_d = 0.0;
+    for (int c = 0; c <= 0x7F; ++c) {
+        if (is_nan_code(F, (uint8_t)c) || is_inf_code(F, (uint8_t)c)) continue;
+        double d = std::fabs(a - decode_exact(F, (uint8_t)c));
+        if (best < 0 || d < best_d || (d == best_d && (c & 1) == 0)) { best = c; best_d = d; }
+    }
+    return (uint8_t)(sign | best);
+}
+
+// bf16 <-> binary32.  bf16 is the upper half of a binary32.
+float bf16_to_f32(uint16_t h) { return bits_f32((uint32_t)h << 16); }
+
+uint16_t f32_to_bf16(float f) {
+    uint32_t u = f32_bits(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x0040u);   // quiet NaN
+    uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1;   // may carry into inf
+    return (uint16_t)keep;
+}
+
+float decode_f(const Fmt& F, uint8_t c) { return (float)decode_exact(F, c); }
+
+}  // namespace
+
+extern "C" {
+
+// ------------------------------------------------------- element codecs --
+uint8_t orc_encode(int fmt, float v) { return encode_bits(fmt_of(fmt), v); }
+uint8_t orc_encode_brute(int fmt, float v) { return encode_brute(fmt_of(fmt), v); }
+float orc_decode(int fmt, uint8_t c) { return decode_f(fmt_of(fmt), c); }
+float orc_fmt_max(int fmt) { return fmt_of(fmt).max_value; }
+
+void orc_encode_array(int fmt, const float* v, size_t n, uint8_t* out) {
+    const Fmt& F = fmt_of(fmt);
+    for (size_t i = 0; i < n; ++i) out[i] = encode_bits(F, v[i]);
+}
+void orc_encode_brute_array(int fmt, const float* v, size_t n, uint8_t* out) {
+    const Fmt& F = fmt_of(fmt);
+    for (size_t i = 0; i < n; ++i) out[i] = encode_brute(F, v[i]);
+}
+// Encodes the binary32 values whose bit patterns are first, first+1, ...
+// (the exhaustive conversion sweep walks all 2^32 patterns this way).
+void orc_encode_pattern_range(int fmt, uint64_t first, size_t n, uint8_t* out) {
+    const Fmt& F = fmt_of(fmt);
+    for (size_t i = 0; i < n; ++i) out[i] = encode_bits(F, bits_f32((uint32_t)(first + i)));
+}
+void orc_decode_array(int fmt, const uint8_t* c, size_t n, float* out) {
+    const Fmt& F = fmt_of(fmt);
+    for (size_t i = 0; i < n; ++i) out[i] = decode_f(F, c[i]);
+}
+void orc_bf16_to_f32_array(const uint16_t* h, size_t n, float* out) {
+    for (size_t i = 0; i < n; ++i) out[i] = bf16_to_f32(h[i]);
+}
+void orc_f32_to_bf16_array(const float* f, size_t n, uint16_t* out) {
+    for (size_t i = 0; i < n; ++i) out[i] = f32_to_bf16(f[i]);
+}
+
+size_t orc_num_blocks(size_t n) { return (n + 127) / 128; }
+
+// ------------------------------------------------ (a) blockwise quantize --
+// [P1] intro ("blockwise scaling") and "FP8 Transmission Optimization and
+// Bottlenecks" (e4m3/e5m2).  Per 128-element block b:
+//   amax = max |x_i|            (bf16 -> binary32 is exact)
+//   s_b  = RN(amax / Fmax)      (Fmax = 448 for e4m3, 57344 for e5m2)
+//   c_i  = satfinite RNE_fp8(RN(x_i / s_b)),  or the signed zero of x_i when s_b == 0.
+void orc_quantize_blockwise(const uint16_t* x, size_t n, int fmt, uint8_t* codes, float* scales) {
+    const Fmt& F = fmt_of(fmt);
+    size_t nb = (n + 127) / 128;
+    for (size_t b = 0; b < nb; ++b) {
+        size_t lo = b * 128, hi = lo + 128 < n ? lo + 128 : n;
+        float amax = 0.0f;
+        for (size_t i = lo; i < hi; ++i) {
+            float a = std::fabs(bf16_to_f32(x[i]));
+            if (a > amax) amax = a;
+        }
+        float s = amax / F.max_value;
+        scales[b] = s;
+        for (size_t i = lo; i < hi; ++i) {
+            float xi = bf16_to_f32(x[i]);
+            float q = (s == 0.0f) ? xi : xi / s;
+            codes[i] = encode_bits(F, q);
+        }
+    }
+}
+
+// ------------------------------------------------------ dequantize --------
+// d_i = RN(decode(c_i) * s_b); the decode itself is exact.
+void orc_dequantize(const uint8_t* codes, const float* scales, size_t n, int fmt,
+                    uint16_t* out_bf16, float* out_f32) {
+    const Fmt& F = fmt_of(fmt);
+    for (size_t i = 0; i < n; ++i) {
+        float d = decode_f(F, codes[i]) * scales[i / 128];
+        if (out_f32) out_f32[i] = d;
+        if (out_bf16) out_bf16[i] = f32_to_bf16(d);
+    }
+}
+
+// ------------------------------------------- (b) fused dequant-reduce -----
+// [P1] "FP8 Transmission Optimization and Bottlenecks": k shards are
+// dequantized and summed without writing the dequantized values out.
+//   acc = +0;  for r = 0..k-1: acc = RN(acc + RN(decode(c_r,i) * s_r,b))
+//   out_f32 = acc,  out_bf16 = RNE_bf16(acc).
+// codes[r] / scales[r] point at shard r.  Either output may be null.
+void orc_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k, size_t n,
+                        int fmt, uint16_t* out_bf16, float* out_f32) {
+    const Fmt& F = fmt_of(fmt);
+    for (size_t i = 0; i < n; ++i) {
+        float acc = 0.0f;
+        for (int r = 0; r < k; ++r) {
+            float d = decode_f(F, codes[r][i]) * scales[r][i / 128];
+            acc = acc + d;
+        }
+        if (out_f32) out_f32[i] = acc;
+        if (out_bf16) out_bf16[i] = f32_to_bf16(acc);
+    }
+}
+
+// ---------------------------------------------------- (c) ring hop --------
+// [P1] ring-based collectives carried on FP8; [P2] ring AllReduce of the
+// bf16 gradients.  One hop at the receiver:
+//   y_i = RN(RN(decode(in_i) * in_s_b) + local_i)
+//   then blockwise quantize of y (amax over |y|, s = RN(amax/Fmax),
+//   c = RNE_fp8(RN(y / s))), and optionally out_bf16 = RNE_bf16(y) (O9).
+void orc_ring_hop(const uint8_t* in_codes, const float* in_scales, const uint16_t* local,
+                  size_t n, int fmt, uint8_t* out_codes, float* out_scales, uint16_t* out_bf16) {
+    const Fmt& F = fmt_of(fmt);
+    size_t nb = (n + 127) / 128;
+    float y[128];
+    for (size_t b = 0; b < nb; ++b) {
+        size_t lo = b * 128, hi = lo + 128 < n ? lo + 128 : n;
+        float amax = 0.0f;
+        for (size_t i = lo; i < hi; ++i) {
+            float d = decode_f(F, in_codes[i]) * in_scales[b];
+            float yi = d + bf16_to_f32(local[i]);
+            y[i - lo] = yi;
+            float a = std::fabs(yi);
+            if (a > amax) amax = a;
+        }
+        float s = amax / F.max_value;
+        out_scales[b] = s;
+        for (size_t i = lo; i < hi; ++i) {
+            float yi = y[i - lo];
+            float q = (s == 0.0f) ? yi : yi / s;
+            out_codes[i] = encode_bits(F, q);
+            if (out_bf16) out_bf16[i] = f32_to_bf16(yi);
+        }
+    }
+}
+
+// --------------------------------------- (d) MXFP8 weight prequantization --
+// [P3] Summary ("Quantize eligible trainer weights before the ... transfer"),
+// self-review ("E8M0 zero-scale clamp", "2D/3D reshape"), [MX] section 6.3.
+// For each row r of each matrix and each 32-element block j along K:
+//   amax = max |w|;  e = 0 if amax == 0 (zero-scale clamp, O12), else
+//   e = clamp(floor(log2 amax) - 8 + 127, 0, 254)   (8 = emax of E4M3)
+//   code = satfinite RNE_e4m3(w * 2^(127 - e)).
+uint8_t orc_e8m0_of_amax(float amax) {
+    if (amax == 0.0f) return 0;
+    int ex = 0;
+    std::frexp((double)amax, &ex);           // amax = f * 2^ex, f in [0.5, 1)
+    int X = (ex - 1) - 8;                     // floor(log2 amax) - emax(E4M3)
+    int e = X + 127;
+    if (e < 0) e = 0;
+    if (e > 254) e = 254;
+    return (uint8_t)e;
+}
+
+// One 32-element block: writes 32 codes, returns the E8M0 byte.
+uint8_t orc_mxfp8_block(const uint16_t* w32, uint8_t* codes32) {
+    float amax = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+        float a = std::fabs(bf16_to_f32(w32[i]));
+        if (a > amax) amax = a;
+    }
+    uint8_t e = orc_e8m0_of_amax(amax);
+    for (int i = 0; i < 32; ++i)
+        codes32[i] = encode_bits(kE4M3, std::ldexp(bf16_to_f32(w32[i]), 127 - (int)e));
+    return e;
+}
+
+// O14: byte offset of scale (r, j) of matrix bt inside the swizzled buffer.
+// Rows are padded to a multiple of 128 and the K/32 scale columns to a
+// multiple of 4; each 128x4 tile is 512 contiguous bytes, tiles are ordered
+// row-tile major, matrices are concatenated.
+uint64_t orc_swizzle_offset(int64_t bt, int64_t r, int64_t j, int64_t m, int64_t kb) {
+    int64_t col_tiles = (kb + 3) / 4;
+    int64_t row_tiles = (m + 127) / 128;
+    int64_t tile = (r / 128) * col_tiles + (j / 4);
+    return (uint64_t)(bt * row_tiles * col_tiles * 512 + tile * 512 + (r % 32) * 16 +
+                      ((r % 128) / 32) * 4 + (j % 4));
+}
+
+uint64_t orc_swizzled_scale_bytes(int64_t batch, int64_t m, int64_t k) {
+    int64_t kb = k / 32;
+    return (uint64_t)(batch * ((m + 127) / 128) * ((kb + 3) / 4) * 512);
+}
+
+// w: [batch, m, k] row-major bf16, k % 32 == 0.  codes: [batch, m, k];
+// scales: orc_swizzled_scale_bytes() bytes, padding written as 0.
+// Returns 0, or -1 when k is not a multiple of 32 (O17).
+int orc_mxfp8_quantize_swizzled(const uint16_t* w, int64_t batch, int64_t m, int64_t k,
+                                uint8_t* codes, uint8_t* scales) {
+    if (k % 32 != 0 || k <= 0) return -1;
+    int64_t kb = k / 32;
+    std::memset(scales, 0, orc_swizzled_scale_bytes(batch, m, k));
+    for (int64_t bt = 0; bt < batch; ++bt)
+        for (int64_t r = 0; r < m; ++r)
+            for (int64_t j = 0; j < kb; ++j) {
+                size_t off = (size_t)((bt * m + r) * k + j * 32);
+                scales[orc_swizzle_offset(bt, r, j, m, kb)] = orc_mxfp8_block(w + off, codes + off);
+            }
+    return 0;
+}
+
+}  // extern "C"
