@@ -1,0 +1,169 @@
+/* fp8q -- FP8 / MXFP8 transfer codec for GB300 (sm_103a).
+ *
+ * C ABI of libfp8q.so.  Every entry point takes plain pointers and sizes,
+ * runs asynchronously on the caller's CUDA stream, allocates nothing, never
+ * synchronizes and never frees.  Arguments are validated on the host before
+ * anything is launched; a failed check returns its status synchronously and
+ * launches nothing.  A launch that the CUDA runtime rejects returns
+ * FP8Q_ERR_CUDA (the runtime's code is kept in fp8q_last_cuda_error()).
+ * No C++ exception crosses this boundary.
+ *
+ * Pointer rules common to all entry points:
+ *  - data pointers are DEVICE pointers owned by the caller, 16-byte aligned
+ *    (FP8Q_ERR_ALIGN otherwise);
+ *  - an output may not overlap an input or another output (FP8Q_ERR_ALIAS),
+ *    except where an entry point says so;
+ *  - bf16 arrays hold IEEE binary32 values truncated to their upper 16 bits
+ *    (the usual bfloat16), passed as `void*`;
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Sources (web pages, cited by title and section):
+ *  [P1] "FP8 Transmission Optimization for VLA Training: Byte Reduction Leads
+ *       to Increased Latency" -- intro ("blockwise scaling", 48.4% fewer wire
+ *       bytes than bf16) and "FP8 Transmission Optimization and Bottlenecks"
+ *       (e4m3/e5m2 conversion kernels; fused dequantize-then-reduce that
+ *       avoids the HBM traffic of the naive order; ring-based collectives).
+ *  [P2] "How to Speed Up VLA Training Step by Step: 3x on Pi0.5" -- PCIe
+ *       paragraph: bf16 gradients reduced by a ring AllReduce.
+ *  [P3] "perf: Reduce MXFP8 refit weight-transfer overheads" -- Summary
+ *       (trainer-side BF16->MXFP8 prequantization, MXFP8 shuffle buffers),
+ *       Safety (each E4M3 tensor travels with its scale), self-review (E8M0
+ *       zero-scale clamp; 2D/3D expert tensors), inline review (a K/32 scale
+ *       dimension of size 1 must survive).
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* fp8q_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    FP8Q_E4M3 = 0, /* OFP8 E4M3 "fn": bias 7, max 448, no inf, 0x7F/0xFF NaN */
+    FP8Q_E5M2 = 1  /* OFP8 E5M2: bias 15, max 57344, IEEE-style inf/NaN      */
+} fp8q_format_t;
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_NULL = 1,   /* a required pointer is NULL                        */
+    FP8Q_ERR_SIZE = 2,   /* a size is negative or beyond FP8Q_MAX_ELEMENTS    */
+    FP8Q_ERR_ALIGN = 3,  /* a pointer is not 16-byte aligned                  */
+    FP8Q_ERR_FORMAT = 4, /* unknown fp8q_format_t                             */
+    FP8Q_ERR_K = 5,      /* shard count outside [1, FP8Q_MAX_SHARDS], or an
+                            MXFP8 K that is not a positive multiple of 32     */
+    FP8Q_ERR_CUDA = 6,   /* the CUDA runtime rejected a launch                */
+    FP8Q_ERR_ALIAS = 7   /* an output overlaps an input or another output     */
+} fp8q_status_t;
+
+#define FP8Q_BLOCK 128                   /* elements per blockwise scale   */
+#define FP8Q_MAX_SHARDS 16               /* k limit of fp8q_dequant_reduce */
+#define FP8Q_MAX_ELEMENTS (1ull << 42)   /* n limit of every entry point   */
+#define MXFP8_BLOCK 32                   /* elements per E8M0 scale        */
+
+/* ---------------------------------------------------------------- (a) ----
+ * Blockwise FP8 quantize ([P1] intro, "FP8 Transmission Optimization and
+ * Bottlenecks").  For each block b of 128 consecutive elements (the last one
+ * may be partial and covers only the valid elements):
+ *     amax_b = max |x_i|,   scales[b] = RN_fp32(amax_b / Fmax)
+ *     codes[i] = satfinite RNE_fp8(RN_fp32(x_i / scales[b]))
+ * with Fmax = 448 (e4m3) or 57344 (e5m2); an all-zero block gets scale 0
+ * and codes equal to the signed zero of each x_i.
+ *   x_bf16 : n bf16 values (in)
+ *   codes  : n bytes (out);  scales : fp8q_num_scales(n) floats (out)
+ * n == 0 is a no-op returning FP8Q_OK. */
+fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, fp8q_format_t fmt,
+                                      uint8_t* codes, float* scales, fp8q_stream_t stream);
+
+/* ---------------------------------------------------------------- (b) ----
+ * Fused k-way dequantize-then-reduce ([P1] "FP8 Transmission Optimization
+ * and Bottlenecks": the fused kernel never writes dequantized shards to
+ * HBM).  For every element i, in rank order r = 0 .. k-1:
+ *     acc = +0;  acc = RN(acc + RN(decode(codes[r][i]) * scales[r][i/128]))
+ *     out_fp32[i] = acc,  out_bf16[i] = RNE_bf16(acc)
+ * A sum, not a mean.
+ *   codes, scales : HOST arrays of k device pointers (shard r: n codes and
+ *                   fp8q_num_scales(n) scales); 1 <= k <= FP8Q_MAX_SHARDS
+ *   out_bf16, out_fp32 : n elements each; either may be NULL, not both. */
+fp8q_status_t fp8q_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k,
+                                  size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
+                                  fp8q_stream_t stream);
+
+/* ---------------------------------------------------------------- (c) ----
+ * One hop of a ring reduction carried on the FP8 wire format ([P1] ring-based
+ * collectives; [P2] ring AllReduce of bf16 gradients).  At the receiver:
+ *     y_i = RN(RN(decode(in_codes[i]) * in_scales[i/128]) + local_i)
+ * then y is quantized blockwise exactly as in (a) (amax over |y|, the fp32
+ * sum itself is requantized, not its bf16 rounding) into out_codes /
+ * out_scales, and, when out_bf16 != NULL, out_bf16[i] = RNE_bf16(y_i).
+ *   in_codes: n bytes; in_scales: fp8q_num_scales(n); local_bf16: n bf16 (in)
+ *   out_codes, out_scales: as in (a) (out); out_bf16: n bf16 or NULL (out)
+ * out_bf16 may be the same pointer as local_bf16 (in-place update of the
+ * local partial); no other overlap is allowed. */
+fp8q_status_t fp8q_ring_hop(const uint8_t* in_codes, const float* in_scales, const void* local_bf16,
+                            size_t n, fp8q_format_t fmt, uint8_t* out_codes, float* out_scales,
+                            void* out_bf16, fp8q_stream_t stream);
+
+/* ---------------------------------------------------------------- (d) ----
+ * BF16 -> MXFP8 weight prequantization ([P3] Summary, self-review).
+ * w is [batch, m, k] row-major ([out, in] weights, batch = experts); every
+ * row is cut into k/32 blocks of 32 along k.  Per block:
+ *     amax = max |w|;  e = 0 if amax == 0 (zero-scale clamp), else
+ *     e = clamp(floor(log2 amax) - 8 + 127, 0, 254)          (E8M0 byte)
+ *     codes = satfinite RNE_e4m3(w * 2^(127 - e))             (row-major)
+ * The E8M0 bytes are written in the 128x4-tiled layout of block-scaled GEMMs:
+ * scale (r, j) of matrix bt lives at
+ *     bt * R * C * 512 + ((r/128) * C + j/4) * 512
+ *        + (r%32) * 16 + ((r%128)/32) * 4 + (j%4)
+ * with R = ceil(m/128), C = ceil((k/32)/4); padding bytes are written as 0.
+ *   codes: batch*m*k bytes; scales_swizzled: mxfp8_swizzled_scale_bytes()
+ * k must be a positive multiple of 32 (FP8Q_ERR_K); k == 32 keeps its one
+ * scale column (padded to 4).  batch == 0 or m == 0 is a no-op. */
+fp8q_status_t mxfp8_quantize_swizzled(const void* w_bf16, int64_t batch, int64_t m, int64_t k,
+                                      uint8_t* codes, uint8_t* scales_swizzled, fp8q_stream_t stream);
+
+/* ------------------------------------------------------------- helpers ---- */
+
+/* ceil(n / 128): the number of fp32 scales of an n-element blockwise array. */
+size_t fp8q_num_scales(size_t n);
+
+/* Bytes of the swizzled E8M0 scale buffer of a [batch, m, k] weight
+ * (0 for invalid arguments). */
+size_t mxfp8_swizzled_scale_bytes(int64_t batch, int64_t m, int64_t k);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fp8q_status_string(fp8q_status_t status);
+
+/* cudaError_t of the most recent FP8Q_ERR_CUDA on the calling thread (0 if none). */
+int fp8q_last_cuda_error(void);
+
+/* Plain satfinite round-to-nearest-even conversion of n binary32 values to
+ * FP8 codes, with no scale (the element conversion step of (a) and (c),
+ * exposed for exhaustive checking and for per-tensor scaled callers).
+ *   x: n floats (in);  codes: n bytes (out). */
+fp8q_status_t fp8q_encode_f32(const float* x, size_t n, fp8q_format_t fmt, uint8_t* codes,
+                              fp8q_stream_t stream);
+
+/* Single-shard dequantize: d_i = RN(decode(codes[i]) * scales[i/128]), written
+ * as fp32 and/or RNE bf16 (either output may be NULL, not both). */
+fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                              void* out_bf16, float* out_fp32, fp8q_stream_t stream);
+
+/* The naive order that (b) replaces ([P1]: "naive dequantize-then-reduce"),
+ * kept as a comparator: each shard is dequantized to fp32 in `workspace`
+ * (k * n floats, caller-owned), then the k fp32 arrays are summed in rank
+ * order.  Bit-identical to fp8q_dequant_reduce; it only moves more bytes. */
+fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const float* const* scales,
+                                          int k, size_t n, fp8q_format_t fmt, float* workspace,
+                                          void* out_bf16, float* out_fp32, fp8q_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

@@ -1,0 +1,145 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/*.h declares, and rejects bad arguments synchronously with the
+documented status before anything is launched.
+
+Every call here fails validation (or is an n == 0 no-op), so no CUDA work is
+ever issued; fake device addresses are never dereferenced.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+OK, ERR_NULL, ERR_SIZE, ERR_ALIGN, ERR_FORMAT, ERR_K, ERR_CUDA, ERR_ALIAS = range(8)
+A = 0x7F0000000000            # a 16-byte aligned fake device address
+MB = 1 << 20
+
+
+@pytest.fixture(scope="module")
+def L():
+    from weight_transfer_gb300 import build
+    build.build()
+    import weight_transfer_gb300 as w
+    return w.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M):
+            if not m.group(0).lstrip().startswith(("typedef", "#", "struct")):
+                names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_function(L):
+    names = declared_functions()
+    expected = {"fp8q_quantize_blockwise", "fp8q_dequant_reduce", "fp8q_ring_hop", "mxfp8_quantize_swizzled",
+                "fp8q_num_scales", "mxfp8_swizzled_scale_bytes", "fp8q_status_string"}
+    assert expected <= names, names
+    for n in sorted(names):
+        assert hasattr(L, n), f"{n} is declared in include/ but not exported"
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert len(L.fp8q_status_string(s)) > 0
+    assert L.fp8q_status_string(0) == b"ok"
+    assert L.fp8q_status_string(99) == b"unknown status"
+
+
+def test_size_helpers(L, orc):
+    for n, nb in [(0, 0), (1, 1), (127, 1), (128, 1), (129, 2), (3_500_000_000, 27_343_750)]:
+        assert L.fp8q_num_scales(n) == nb
+    for b, m, k in [(1, 256, 256), (2, 129, 32), (128, 768, 2048), (1, 2048, 4096), (3, 1, 96)]:
+        assert L.mxfp8_swizzled_scale_bytes(b, m, k) == orc.swizzled_scale_bytes(b, m, k)
+    assert L.mxfp8_swizzled_scale_bytes(1, 128, 48) == 0
+
+
+def test_quantize_validation(L):
+    q = L.fp8q_quantize_blockwise
+    assert q(A, 1024, 5, A + MB, A + 2 * MB, None) == ERR_FORMAT
+    assert q(A, (1 << 42) + 1, 0, A + MB, A + 2 * MB, None) == ERR_SIZE
+    assert q(None, 0, 0, None, None, None) == OK                      # empty: no-op
+    assert q(None, 1024, 0, A + MB, A + 2 * MB, None) == ERR_NULL
+    assert q(A, 1024, 0, None, A + 2 * MB, None) == ERR_NULL
+    assert q(A + 2, 1024, 0, A + MB, A + 2 * MB, None) == ERR_ALIGN
+    assert q(A, 1024, 0, A + MB + 8, A + 2 * MB, None) == ERR_ALIGN
+    assert q(A, 1024, 0, A + 1024, A + 2 * MB, None) == ERR_ALIAS     # codes inside x
+    assert q(A, 1024, 1, A + MB, A + MB + 512, None) == ERR_ALIAS     # scales inside codes
+
+
+def _ptrs(vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def test_dequant_reduce_validation(L):
+    r = L.fp8q_dequant_reduce
+    c = _ptrs([A + i * MB for i in range(17)])
+    s = _ptrs([A + 64 * MB + i * MB for i in range(17)])
+    ob, of = A + 200 * MB, A + 300 * MB
+    assert r(c, s, 0, 1024, 0, ob, of, None) == ERR_K
+    assert r(c, s, 17, 1024, 0, ob, of, None) == ERR_K
+    assert r(c, s, 2, 1024, 3, ob, of, None) == ERR_FORMAT
+    assert r(c, s, 2, 1024, 0, None, None, None) == ERR_NULL
+    assert r(None, s, 2, 1024, 0, ob, of, None) == ERR_NULL
+    assert r(_ptrs([A, 0]), s, 2, 1024, 0, ob, of, None) == ERR_NULL
+    assert r(c, s, 2, 0, 0, ob, of, None) == OK
+    assert r(_ptrs([A, A + MB + 4]), s, 2, 1024, 0, ob, of, None) == ERR_ALIGN
+    assert r(c, s, 2, 1024, 0, ob + 2, of, None) == ERR_ALIGN
+    assert r(c, s, 2, 1024, 0, c[1], None, None) == ERR_ALIAS         # output over shard 1 codes
+    assert r(c, s, 2, 1024, 0, ob, ob + 1024, None) == ERR_ALIAS       # the two outputs overlap
+    assert r(c, s, 2, 1 << 43, 0, ob, of, None) == ERR_SIZE
+
+
+def test_ring_hop_validation(L):
+    h = L.fp8q_ring_hop
+    ic, isc, loc, oc, osc, ob = (A + i * MB for i in range(6))
+    assert h(ic, isc, loc, 1024, 2, oc, osc, ob, None) == ERR_FORMAT
+    assert h(ic, isc, None, 1024, 0, oc, osc, ob, None) == ERR_NULL
+    assert h(ic, isc, loc, 1024, 0, None, osc, ob, None) == ERR_NULL
+    assert h(ic, isc, loc + 4, 1024, 0, oc, osc, ob, None) == ERR_ALIGN
+    assert h(ic, isc, loc, 1024, 0, ic, osc, ob, None) == ERR_ALIAS     # out codes over in codes
+    assert h(ic, isc, loc, 1024, 0, oc, osc, oc, None) == ERR_ALIAS     # bf16 out over out codes
+    assert h(ic, isc, loc, 1024, 0, oc, osc, loc + 16, None) == ERR_ALIAS  # partial overlap with local
+    assert h(ic, isc, loc, 0, 0, oc, osc, ob, None) == OK
+
+
+def test_mxfp8_validation(L):
+    f = L.mxfp8_quantize_swizzled
+    w, c, s = A, A + 64 * MB, A + 128 * MB
+    assert f(w, 1, 128, 48, c, s, None) == ERR_K
+    assert f(w, 1, 128, 0, c, s, None) == ERR_K
+    assert f(w, 1, 128, -32, c, s, None) == ERR_K
+    assert f(w, -1, 128, 64, c, s, None) == ERR_SIZE
+    assert f(w, 1, -5, 64, c, s, None) == ERR_SIZE
+    assert f(w, 0, 128, 64, c, s, None) == OK
+    assert f(w, 1, 0, 64, c, s, None) == OK
+    assert f(None, 1, 128, 64, c, s, None) == ERR_NULL
+    assert f(w + 8, 1, 128, 64, c, s, None) == ERR_ALIGN
+    assert f(w, 1, 128, 64, w + 64, s, None) == ERR_ALIAS
+    assert f(w, 1 << 20, 1 << 20, 1 << 20, c, s, None) == ERR_SIZE
+
+
+def test_other_entry_points_validation(L):
+    assert L.fp8q_encode_f32(A, 100, 9, A + MB, None) == ERR_FORMAT
+    assert L.fp8q_encode_f32(A, 100, 0, A + 192, None) == ERR_ALIAS
+    assert L.fp8q_dequantize(A, A + MB, 100, 0, None, None, None) == ERR_NULL
+    c = _ptrs([A, A + MB])
+    s = _ptrs([A + 2 * MB, A + 3 * MB])
+    assert L.fp8q_dequant_reduce_unfused(c, s, 2, 1024, 0, None, A + 4 * MB, None, None) == ERR_NULL
+    assert L.fp8q_dequant_reduce_unfused(c, s, 2, 1024, 0, A + 4 * MB, A + 4 * MB, None, None) == ERR_ALIAS
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    import weight_transfer_gb300 as w
+    with pytest.raises(ValueError):
+        w.fp8q_quantize_blockwise(torch.zeros(256, dtype=torch.bfloat16),
+                                  codes=torch.zeros(1), scales=torch.zeros(1))

@@ -1,0 +1,101 @@
+"""(d) BF16 -> MXFP8 prequantization with the swizzled E8M0 scales on the
+GPU, against the oracle: codes and the whole scale buffer (padding
+included) bit for bit."""
+import concurrent.futures as cf
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+from gpu_util import Guarded, assert_same, bf16_from_bits, bits16, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w():
+    import weight_transfer_gb300 as w
+    return w
+
+
+def weight_bits(b, m, k, seed):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((b, m, k)) * 0.02).astype(np.float32)
+    rows = rng.random((b, m)) < 0.05
+    x[rows] *= 50.0
+    blk = x.reshape(b, m, k // 32, 32)
+    z = rng.random((b, m, k // 32)) < 0.03
+    blk[z] = 0.0                                           # zero-scale clamp
+    t = rng.random((b, m, k // 32)) < 0.02
+    blk[t] *= 1e-36                                        # tiny / subnormal blocks
+    h = rng.random((b, m, k // 32)) < 0.01
+    blk[h] *= 1e30                                         # huge blocks
+    bits = torch.from_numpy(x.ravel()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    if bits.size > 64:
+        bits[7] = 0x7F7F                                   # largest bf16
+        bits[40] = 0x8000                                  # negative zero
+    bits[(bits & 0x7F80) == 0x7F80] = 0x3C00
+    return bits
+
+
+def run(w, bits, b, m, k):
+    x = bf16_from_bits(bits).view(b, m, k)
+    gc = Guarded(b * m * k, torch.uint8)
+    sb = w.mxfp8_swizzled_scale_bytes(b, m, k)
+    gs = Guarded(sb, torch.uint8)
+    w.mxfp8_quantize_swizzled(x, codes=gc.t.view(b, m, k), scales_swizzled=gs.t)
+    torch.cuda.synchronize()
+    assert gc.intact() and gs.intact(), "write outside the output buffers"
+    return u8(gc.t), u8(gs.t)
+
+
+@pytest.mark.parametrize("b,m,k", [(1, 1, 32), (1, 1, 64), (1, 127, 64), (1, 128, 128), (1, 129, 96), (3, 129, 32),
+                                   (2, 256, 768), (1, 300, 2048), (5, 64, 160), (1, 4096, 2048), (2, 768, 2048)])
+def test_mxfp8_shapes(w, orc, b, m, k):
+    bits = weight_bits(b, m, k, seed=b * 7 + m + k)
+    gc, gs = run(w, bits, b, m, k)
+    ec, es = orc.mxfp8_quantize_swizzled(bits, b, m, k)
+    assert_same(gs, es, "swizzled scales")
+    assert_same(gc, ec, "codes")
+
+
+def test_mxfp8_k32_scale_column_survives(w, orc):
+    # K == 32: one real scale column per row, padded to a 4-wide tile
+    bits = weight_bits(1, 200, 32, seed=5)
+    gc, gs = run(w, bits, 1, 200, 32)
+    ec, es = orc.mxfp8_quantize_swizzled(bits, 1, 200, 32)
+    assert gs.size == 2 * 512
+    assert_same(gs, es, "scales")
+    assert_same(gc, ec, "codes")
+
+
+def test_mxfp8_2d_call(w, orc):
+    bits = weight_bits(1, 256, 512, seed=11)
+    c, s = w.mxfp8_quantize_swizzled(bf16_from_bits(bits).view(256, 512))
+    ec, es = orc.mxfp8_quantize_swizzled(bits, 1, 256, 512)
+    assert c.shape == (256, 512)
+    assert_same(u8(c).ravel(), ec, "codes")
+    assert_same(u8(s), es, "scales")
+
+
+def test_mxfp8_qwen3_layer_full_size(w, orc):
+    # every tensor of one Qwen3-30B-A3B-shaped layer (all 48 layers have the
+    # same shapes), checked in full; the oracle runs on expert slices in
+    # parallel (the swizzled buffer is a concatenation over the batch)
+    pool = cf.ThreadPoolExecutor(16)
+    for t, (name, b, m, k) in enumerate(gen.QWEN3_TENSORS):
+        x = gen.qwen3_tensor(0, t)
+        c, s = w.mxfp8_quantize_swizzled(x.cuda())
+        hb = bits16(x).reshape(b, m * k)
+        per = w.mxfp8_swizzled_scale_bytes(1, m, k)
+        step = max(1, b // 16)
+        jobs = [(i, min(b, i + step)) for i in range(0, b, step)]
+        res = list(pool.map(lambda ij: orc.mxfp8_quantize_swizzled(hb[ij[0]:ij[1]].copy(), ij[1] - ij[0], m, k), jobs))
+        ec = np.concatenate([r[0] for r in res])
+        es = np.concatenate([r[1] for r in res])
+        assert es.size == b * per
+        assert_same(u8(s), es, f"{name} scales")
+        assert_same(u8(c).ravel(), ec, f"{name} codes")
+        del c, s, x
+    pool.shutdown()

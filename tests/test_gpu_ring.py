@@ -1,0 +1,106 @@
+"""(c) The ring hop on the GPU against the oracle: single hops on adversarial
+inputs, and the 7-hop chain of a ring of 8 over the payload sweep."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+from gpu_util import Guarded, assert_same, assert_same_f32, bf16_from_bits, bits16, u8, varied_bf16
+from test_gpu_reduce import random_shards
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w():
+    import weight_transfer_gb300 as w
+    return w
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("n", [1, 15, 16, 17, 127, 128, 129, 4096 + 17, 200_003])
+@pytest.mark.parametrize("with_bf16", [True, False])
+def test_single_hop(w, orc, fmt, n, with_bf16):
+    codes, scales = random_shards(1, n, fmt, seed=n + 17 * fmt)
+    # keep the incoming values in a range where adding the local partial
+    # stays finite
+    scales[0] = np.minimum(scales[0], np.float32(1e20))
+    loc = varied_bf16(n, seed=n + 5)
+    gc = Guarded(n, torch.uint8)
+    gs = Guarded((n + 127) // 128, torch.float32)
+    gb = Guarded(n, torch.bfloat16) if with_bf16 else None
+    w.fp8q_ring_hop(torch.from_numpy(codes[0]).cuda(), torch.from_numpy(scales[0]).cuda(), bf16_from_bits(loc), fmt,
+                    out_codes=gc.t, out_scales=gs.t, out_bf16=gb.t if gb else None)
+    torch.cuda.synchronize()
+    assert gc.intact() and gs.intact() and (gb is None or gb.intact())
+    oc, os_, ob = orc.ring_hop(codes[0], scales[0], loc, fmt)
+    assert_same_f32(gs.t.cpu().numpy(), os_, "scales")
+    assert_same(u8(gc.t), oc, "codes")
+    if gb:
+        assert_same(bits16(gb.t), ob, "bf16")
+
+
+def test_hop_in_place_local_update(w, orc):
+    n = 100_000
+    codes, scales = random_shards(1, n, 0, seed=4)
+    scales[0] = np.minimum(scales[0], np.float32(1e20))
+    loc = varied_bf16(n, seed=9)
+    dloc = bf16_from_bits(loc)
+    oc, os_, ob = w.fp8q_ring_hop(torch.from_numpy(codes[0]).cuda(), torch.from_numpy(scales[0]).cuda(), dloc, 0,
+                                  out_bf16=dloc)
+    ec, es, eb = orc.ring_hop(codes[0], scales[0], loc, 0)
+    assert_same(bits16(dloc), eb, "in-place bf16")
+    assert_same(u8(oc), ec, "codes")
+
+
+def run_chain_gpu(w, parts, fmt):
+    """hop 0 = quantize of partial 0; hops 1..7 add partials 1..7; the last
+    hop also writes bf16.  Returns per-hop (codes, scales) and the final bf16."""
+    hops = [w.fp8q_quantize_blockwise(parts[0], fmt)]
+    last = None
+    for h in range(1, len(parts)):
+        c, s, b = w.fp8q_ring_hop(hops[-1][0], hops[-1][1], parts[h], fmt, want_bf16=h == len(parts) - 1)
+        hops.append((c, s))
+        last = b
+    return hops, last
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("payload", [1 << 10, 1 << 12, 1 << 16, 767 * 1024, 1 << 22, 1 << 24])
+def test_ring_chain_full_check(w, orc, fmt, payload):
+    n = payload // 2
+    host = [gen.ring_partial(r, n) for r in range(gen.RING_PARTIALS)]
+    hops, last = run_chain_gpu(w, [p.cuda() for p in host], fmt)
+    c, s = orc.quantize_blockwise(bits16(host[0]), fmt)
+    for h in range(1, gen.RING_PARTIALS):
+        assert_same(u8(hops[h - 1][0]), c, f"codes after hop {h - 1}")
+        assert_same_f32(hops[h - 1][1].cpu().numpy(), s, f"scales after hop {h - 1}")
+        c, s, b = orc.ring_hop(c, s, bits16(host[h]), fmt)
+    assert_same(u8(hops[-1][0]), c, "final codes")
+    assert_same(bits16(last), b, "final bf16")
+
+
+@pytest.mark.parametrize("payload", [1 << 26, 1 << 28])
+def test_ring_chain_large_sampled(w, orc, payload):
+    # 64 MiB and 256 MiB per-hop payloads, checked on sampled 128-blocks:
+    # every hop is block-local, so the oracle replays the chain of a block
+    # from that block's slice of the 8 partials
+    n = payload // 2
+    host = [gen.ring_partial(r, n) for r in range(gen.RING_PARTIALS)]
+    hops, last = run_chain_gpu(w, [p.cuda() for p in host], 0)
+    nb = n // 128
+    rng = np.random.default_rng(payload >> 20)
+    blocks = np.unique(np.concatenate([rng.integers(0, nb, 400), [0, nb - 1]]))
+    hb = [bits16(p) for p in host]
+    gpu_codes = [u8(c) for c, _ in hops]
+    gpu_scales = [s.cpu().numpy() for _, s in hops]
+    gpu_last = bits16(last)
+    for b in blocks:
+        sl = slice(128 * b, 128 * b + 128)
+        c, s = orc.quantize_blockwise(hb[0][sl].copy(), 0)
+        for h in range(1, gen.RING_PARTIALS):
+            assert_same(gpu_codes[h - 1][sl], c, f"block {b} hop {h - 1}")
+            assert gpu_scales[h - 1][b] == s[0]
+            c, s, bf = orc.ring_hop(c, s, hb[h][sl].copy(), 0)
+        assert_same(gpu_codes[-1][sl], c, f"block {b} final")
+        assert_same(gpu_last[sl], bf, f"block {b} bf16")

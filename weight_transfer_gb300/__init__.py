@@ -1,0 +1,263 @@
+"""weight_transfer_gb300 -- FP8 / MXFP8 transfer codec for GB300 (sm_103a).
+
+Thin Python binding of ``libfp8q.so`` (C ABI declared in ``include/fp8q.h``).
+The functions carry the C names; each one only marshals torch CUDA tensors
+into device pointers, sizes and the current CUDA stream, calls the library,
+and raises ``Fp8qError`` on a non-zero status.  All arithmetic runs in the
+library's CUDA kernels; there is no CPU path.  Outputs may be passed in
+(reused, caller-owned buffers) or are allocated with torch when omitted.
+
+Importing the package loads the library and fails loudly if it has not been
+built (``python -m weight_transfer_gb300.build`` or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8q.so")
+
+FP8Q_E4M3 = 0
+FP8Q_E5M2 = 1
+FORMATS = {"e4m3": FP8Q_E4M3, "e5m2": FP8Q_E5M2}
+FP8Q_MAX_SHARDS = 16
+FP8Q_BLOCK = 128
+MXFP8_BLOCK = 32
+
+STATUS = {0: "FP8Q_OK", 1: "FP8Q_ERR_NULL", 2: "FP8Q_ERR_SIZE", 3: "FP8Q_ERR_ALIGN", 4: "FP8Q_ERR_FORMAT",
+          5: "FP8Q_ERR_K", 6: "FP8Q_ERR_CUDA", 7: "FP8Q_ERR_ALIAS"}
+
+
+class Fp8qError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        extra = f" (cudaError {cuda_error})" if status == 6 else ""
+        super().__init__(f"{fn}: {STATUS.get(status, status)}: {msg}{extra}")
+
+
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+
+# name -> (argtypes, restype)
+_SIGNATURES = {
+    "fp8q_quantize_blockwise": ([_vp, _sz, _int, _vp, _vp, _vp], _int),
+    "fp8q_dequant_reduce": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, _vp], _int),
+    "fp8q_ring_hop": ([_vp, _vp, _vp, _sz, _int, _vp, _vp, _vp, _vp], _int),
+    "mxfp8_quantize_swizzled": ([_vp, _i64, _i64, _i64, _vp, _vp, _vp], _int),
+    "fp8q_num_scales": ([_sz], _sz),
+    "mxfp8_swizzled_scale_bytes": ([_i64, _i64, _i64], _sz),
+    "fp8q_status_string": ([_int], ctypes.c_char_p),
+    "fp8q_last_cuda_error": ([], _int),
+    "fp8q_encode_f32": ([_vp, _sz, _int, _vp, _vp], _int),
+    "fp8q_dequantize": ([_vp, _vp, _sz, _int, _vp, _vp, _vp], _int),
+    "fp8q_dequant_reduce_unfused": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, _vp, _vp],
+                                    _int),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with `python -m weight_transfer_gb300.build`; "
+                              "this package has no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+lib()   # fail at import, not at the first call
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        L = lib()
+        raise Fp8qError(fn, status, L.fp8q_status_string(status).decode(), L.fp8q_last_cuda_error())
+
+
+def _fmt(fmt) -> int:
+    if isinstance(fmt, str):
+        return FORMATS[fmt]
+    return int(fmt)
+
+
+def _dev(t: Optional[torch.Tensor], what: str, dtype=None, numel: Optional[int] = None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{what} holds {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def fp8q_num_scales(n: int) -> int:
+    return int(lib().fp8q_num_scales(n))
+
+
+def mxfp8_swizzled_scale_bytes(batch: int, m: int, k: int) -> int:
+    return int(lib().mxfp8_swizzled_scale_bytes(batch, m, k))
+
+
+def fp8q_quantize_blockwise(x: torch.Tensor, fmt="e4m3", codes: Optional[torch.Tensor] = None,
+                            scales: Optional[torch.Tensor] = None, stream=None):
+    """bf16 x -> (codes uint8 [n], scales float32 [ceil(n/128)])."""
+    n = x.numel()
+    if codes is None:
+        codes = torch.empty(n, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(max(fp8q_num_scales(n), 1), dtype=torch.float32, device=x.device)
+    st = lib().fp8q_quantize_blockwise(_dev(x, "x", torch.bfloat16), n, _fmt(fmt), _dev(codes, "codes", torch.uint8, n),
+                                       _dev(scales, "scales", torch.float32, fp8q_num_scales(n)), _stream(stream))
+    _check("fp8q_quantize_blockwise", st)
+    return codes, scales
+
+
+def _ptr_array(ts: Sequence[torch.Tensor], what: str, dtype, numel: int):
+    arr = (_vp * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _dev(t, f"{what}[{i}]", dtype, numel)
+    return arr
+
+
+def fp8q_dequant_reduce(codes: Sequence[torch.Tensor], scales: Sequence[torch.Tensor], fmt="e4m3",
+                        out_bf16: Optional[torch.Tensor] = None, out_fp32: Optional[torch.Tensor] = None,
+                        want_bf16: bool = True, want_fp32: bool = True, n: Optional[int] = None, stream=None):
+    """Sum of k FP8 shards in rank order -> (bf16 [n] or None, fp32 [n] or None)."""
+    k = len(codes)
+    if k != len(scales):
+        raise ValueError("codes and scales must have the same length")
+    if n is None:
+        n = codes[0].numel()
+    dev = codes[0].device
+    if out_bf16 is None and want_bf16:
+        out_bf16 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    if out_fp32 is None and want_fp32:
+        out_fp32 = torch.empty(n, dtype=torch.float32, device=dev)
+    cp = _ptr_array(codes, "codes", torch.uint8, n)
+    sp = _ptr_array(scales, "scales", torch.float32, fp8q_num_scales(n))
+    st = lib().fp8q_dequant_reduce(cp, sp, k, n, _fmt(fmt), _dev(out_bf16, "out_bf16", torch.bfloat16, n),
+                                   _dev(out_fp32, "out_fp32", torch.float32, n), _stream(stream))
+    _check("fp8q_dequant_reduce", st)
+    return out_bf16, out_fp32
+
+
+def fp8q_ring_hop(in_codes: torch.Tensor, in_scales: torch.Tensor, local: torch.Tensor, fmt="e4m3",
+                  out_codes: Optional[torch.Tensor] = None, out_scales: Optional[torch.Tensor] = None,
+                  out_bf16: Optional[torch.Tensor] = None, want_bf16: bool = False, stream=None):
+    """-> (out_codes, out_scales, out_bf16 or None).  out_bf16 may be `local` (in place)."""
+    n = local.numel()
+    dev = local.device
+    if out_codes is None:
+        out_codes = torch.empty(n, dtype=torch.uint8, device=dev)
+    if out_scales is None:
+        out_scales = torch.empty(max(fp8q_num_scales(n), 1), dtype=torch.float32, device=dev)
+    if out_bf16 is None and want_bf16:
+        out_bf16 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    nb = fp8q_num_scales(n)
+    st = lib().fp8q_ring_hop(_dev(in_codes, "in_codes", torch.uint8, n), _dev(in_scales, "in_scales", torch.float32, nb),
+                             _dev(local, "local", torch.bfloat16), n, _fmt(fmt),
+                             _dev(out_codes, "out_codes", torch.uint8, n),
+                             _dev(out_scales, "out_scales", torch.float32, nb),
+                             _dev(out_bf16, "out_bf16", torch.bfloat16, n), _stream(stream))
+    _check("fp8q_ring_hop", st)
+    return out_codes, out_scales, out_bf16
+
+
+def mxfp8_quantize_swizzled(w: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                            scales_swizzled: Optional[torch.Tensor] = None, stream=None):
+    """bf16 w [m, k] or [batch, m, k] -> (E4M3 codes uint8 same shape, swizzled E8M0 bytes uint8)."""
+    if w.dim() == 2:
+        batch, (m, k) = 1, w.shape
+    elif w.dim() == 3:
+        batch, m, k = w.shape
+    else:
+        raise ValueError("w must be 2D [m, k] or 3D [batch, m, k]")
+    dev = w.device
+    sb = mxfp8_swizzled_scale_bytes(batch, m, k)
+    if codes is None:
+        codes = torch.empty(w.shape, dtype=torch.uint8, device=dev)
+    if scales_swizzled is None:
+        scales_swizzled = torch.empty(max(sb, 16), dtype=torch.uint8, device=dev)
+    st = lib().mxfp8_quantize_swizzled(_dev(w, "w", torch.bfloat16), batch, m, k,
+                                       _dev(codes, "codes", torch.uint8, batch * m * k),
+                                       _dev(scales_swizzled, "scales_swizzled", torch.uint8, sb), _stream(stream))
+    _check("mxfp8_quantize_swizzled", st)
+    return codes, scales_swizzled[:sb]
+
+
+def fp8q_encode_f32(x: torch.Tensor, fmt="e4m3", codes: Optional[torch.Tensor] = None, stream=None):
+    n = x.numel()
+    if codes is None:
+        codes = torch.empty(n, dtype=torch.uint8, device=x.device)
+    st = lib().fp8q_encode_f32(_dev(x, "x", torch.float32), n, _fmt(fmt), _dev(codes, "codes", torch.uint8, n),
+                               _stream(stream))
+    _check("fp8q_encode_f32", st)
+    return codes
+
+
+def fp8q_dequantize(codes: torch.Tensor, scales: torch.Tensor, fmt="e4m3", out_bf16: Optional[torch.Tensor] = None,
+                    out_fp32: Optional[torch.Tensor] = None, want_bf16: bool = False, want_fp32: bool = True,
+                    stream=None):
+    n = codes.numel()
+    dev = codes.device
+    if out_bf16 is None and want_bf16:
+        out_bf16 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    if out_fp32 is None and want_fp32:
+        out_fp32 = torch.empty(n, dtype=torch.float32, device=dev)
+    st = lib().fp8q_dequantize(_dev(codes, "codes", torch.uint8, n),
+                               _dev(scales, "scales", torch.float32, fp8q_num_scales(n)), n, _fmt(fmt),
+                               _dev(out_bf16, "out_bf16", torch.bfloat16, n), _dev(out_fp32, "out_fp32", torch.float32, n),
+                               _stream(stream))
+    _check("fp8q_dequantize", st)
+    return out_bf16, out_fp32
+
+
+def fp8q_dequant_reduce_unfused(codes: Sequence[torch.Tensor], scales: Sequence[torch.Tensor], fmt="e4m3",
+                                workspace: Optional[torch.Tensor] = None, out_bf16: Optional[torch.Tensor] = None,
+                                out_fp32: Optional[torch.Tensor] = None, want_bf16: bool = True,
+                                want_fp32: bool = True, n: Optional[int] = None, stream=None):
+    """The naive dequantize-to-HBM-then-reduce order (comparator); needs a k*n fp32 workspace."""
+    k = len(codes)
+    if n is None:
+        n = codes[0].numel()
+    dev = codes[0].device
+    if workspace is None:
+        workspace = torch.empty(k * n, dtype=torch.float32, device=dev)
+    if out_bf16 is None and want_bf16:
+        out_bf16 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    if out_fp32 is None and want_fp32:
+        out_fp32 = torch.empty(n, dtype=torch.float32, device=dev)
+    cp = _ptr_array(codes, "codes", torch.uint8, n)
+    sp = _ptr_array(scales, "scales", torch.float32, fp8q_num_scales(n))
+    st = lib().fp8q_dequant_reduce_unfused(cp, sp, k, n, _fmt(fmt), _dev(workspace, "workspace", torch.float32, k * n),
+                                           _dev(out_bf16, "out_bf16", torch.bfloat16, n),
+                                           _dev(out_fp32, "out_fp32", torch.float32, n), _stream(stream))
+    _check("fp8q_dequant_reduce_unfused", st)
+    return out_bf16, out_fp32

@@ -1,0 +1,44 @@
+// Entry points with no kernel of their own: size helpers, status strings,
+// CUDA error capture and the cached device query used for launch sizing.
+#include "fp8q_host.cuh"
+
+namespace fp8q {
+
+static thread_local int g_last_cuda_error = 0;
+
+fp8q_status_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FP8Q_OK;
+    g_last_cuda_error = (int)e;
+    return FP8Q_ERR_CUDA;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+}  // namespace fp8q
+
+extern "C" size_t fp8q_num_scales(size_t n) { return n / FP8Q_BLOCK + (n % FP8Q_BLOCK != 0); }
+
+extern "C" int fp8q_last_cuda_error(void) { return fp8q::g_last_cuda_error; }
+
+extern "C" const char* fp8q_status_string(fp8q_status_t status) {
+    switch (status) {
+        case FP8Q_OK: return "ok";
+        case FP8Q_ERR_NULL: return "a required pointer is NULL";
+        case FP8Q_ERR_SIZE: return "size out of range";
+        case FP8Q_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case FP8Q_ERR_FORMAT: return "unknown FP8 format";
+        case FP8Q_ERR_K: return "shard count or MXFP8 K out of range";
+        case FP8Q_ERR_CUDA: return "CUDA launch error (see fp8q_last_cuda_error)";
+        case FP8Q_ERR_ALIAS: return "an output overlaps an input or another output";
+    }
+    return "unknown status";
+}

@@ -1,0 +1,49 @@
+// Host-side helpers shared by the fp8q entry points: argument checks that
+// run before any launch, launch sizing, and CUDA error capture.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "fp8q.h"
+
+namespace fp8q {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [a, a+na) and [b, b+nb) overlap (empty ranges never do).
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+inline bool valid_fmt(fp8q_format_t f) { return f == FP8Q_E4M3 || f == FP8Q_E5M2; }
+
+// Records and maps a CUDA error (thread-local, see fp8q_last_cuda_error).
+fp8q_status_t cuda_status(cudaError_t e);
+
+// Status of the launch just made on this thread.
+inline fp8q_status_t launch_status() { return cuda_status(cudaGetLastError()); }
+
+// SM count of the current device (cached per device).
+int sm_count();
+
+// Blocks of `threads` threads of `kernel` that fit on one SM (cached by the caller).
+template <class K>
+int resident_blocks(K kernel, int threads, size_t smem = 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+    return n;
+}
+
+// Persistent grid: enough blocks to fill every SM `resident` deep, but never
+// more than there is work for.
+inline unsigned grid_for(size_t work_blocks, int resident) {
+    size_t cap = (size_t)sm_count() * (size_t)(resident > 0 ? resident : 1);
+    size_t g = work_blocks < cap ? work_blocks : cap;
+    return (unsigned)(g > 0 ? g : 1);
+}
+
+}  // namespace fp8q

@@ -1,0 +1,241 @@
+// (b) Fused k-way dequantize-then-reduce, single-shard dequantize, and the
+// naive two-pass order kept as a comparator.
+//
+// "FP8 Transmission Optimization for VLA Training", section "FP8
+// Transmission Optimization and Bottlenecks": the naive order dequantizes
+// every shard to HBM and reduces afterwards; the fused kernel reads each
+// shard's codes and scales once and keeps the running sum in registers.
+//
+// Work split: a lane owns 16 consecutive elements (one 16-byte load of codes
+// per shard), 8 lanes cover one 128-element block.  All k shard loads of a
+// lane are issued before the first is decoded (k independent 16-byte loads
+// in flight per lane), then the sum runs in rank order 0..k-1:
+//   acc = +0;  acc = RN(acc + RN(decode(c_r) * s_r))
+// with explicit _rn intrinsics so nothing is fused into an FMA.
+#include "fp8q_device.cuh"
+#include "fp8q_host.cuh"
+
+namespace fp8q {
+
+constexpr int kRedThreads = 256;
+
+struct ShardPtrs {
+    const uint8_t* codes[FP8Q_MAX_SHARDS];
+    const float* scales[FP8Q_MAX_SHARDS];
+};
+
+// Writes 16 results: fp32 as four 16-byte stores, bf16 as two.
+template <bool OUT_BF16, bool OUT_F32>
+__device__ __forceinline__ void store16(const float (&acc)[16], size_t e0, size_t n, uint16_t* out_bf16,
+                                        float* out_f32) {
+    const bool full = e0 + 16 <= n;
+    if (OUT_F32) {
+        if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                st_stream(out_f32 + e0 + 4 * q, make_uint4(__float_as_uint(acc[4 * q]), __float_as_uint(acc[4 * q + 1]),
+                                                           __float_as_uint(acc[4 * q + 2]),
+                                                           __float_as_uint(acc[4 * q + 3])));
+        } else {
+            st_f32_tail(out_f32 + e0, acc, 16, (long long)n - (long long)e0);
+        }
+    }
+    if (OUT_BF16) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+        if (full) {
+            st_stream(out_bf16 + e0, make_uint4(w[0], w[1], w[2], w[3]));
+            st_stream(out_bf16 + e0 + 8, make_uint4(w[4], w[5], w[6], w[7]));
+        } else {
+            st_u16_tail(out_bf16 + e0, w, 8, (long long)n - (long long)e0);
+        }
+    }
+}
+
+// SUM = true: acc starts at +0 and every shard is added (the reduce).
+// SUM = false: k == 1 and the dequantized value is written as is (dequantize).
+template <int FMT, bool OUT_BF16, bool OUT_F32, bool SUM>
+__global__ void __launch_bounds__(kRedThreads)
+dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32) {
+    const size_t units = (n + 15) >> 4;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const size_t e0 = u << 4;
+        const size_t b = u >> 3;
+        const bool full = e0 + 16 <= n;
+        uint4 cv[FP8Q_MAX_SHARDS];
+        float sv[FP8Q_MAX_SHARDS];
+#pragma unroll
+        for (int r = 0; r < FP8Q_MAX_SHARDS; ++r) {
+            if (r < k) {
+                cv[r] = full ? ld_stream(sh.codes[r] + e0) : ld_u8x16_tail(sh.codes[r] + e0, (long long)n - (long long)e0);
+                sv[r] = ld_stream_f32(sh.scales[r] + b);
+            }
+        }
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int r = 0; r < FP8Q_MAX_SHARDS; ++r) {
+            if (r < k) {
+                float d[16];
+                decode_fp8x4<FMT>(cv[r].x, d);
+                decode_fp8x4<FMT>(cv[r].y, d + 4);
+                decode_fp8x4<FMT>(cv[r].z, d + 8);
+                decode_fp8x4<FMT>(cv[r].w, d + 12);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p = __fmul_rn(d[i], sv[r]);
+                    acc[i] = SUM ? __fadd_rn(acc[i], p) : p;
+                }
+            }
+        }
+        store16<OUT_BF16, OUT_F32>(acc, e0, n, out_bf16, out_f32);
+    }
+}
+
+// Second pass of the naive order: k fp32 arrays (stride n apart) summed in
+// rank order from +0.
+template <bool OUT_BF16, bool OUT_F32>
+__global__ void __launch_bounds__(kRedThreads)
+sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, uint16_t* __restrict__ out_bf16,
+               float* __restrict__ out_f32) {
+    const size_t units = (n + 15) >> 4;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+        const size_t e0 = u << 4;
+        const bool full = e0 + 16 <= n;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int r = 0; r < k; ++r) {
+            const float* p = ws + (size_t)r * n + e0;
+            float v[16];
+            if (full && ((reinterpret_cast<uintptr_t>(p) & 15u) == 0)) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 t = ld_stream(p + 4 * q);
+                    v[4 * q] = __uint_as_float(t.x); v[4 * q + 1] = __uint_as_float(t.y);
+                    v[4 * q + 2] = __uint_as_float(t.z); v[4 * q + 3] = __uint_as_float(t.w);
+                }
+            } else {
+                for (int i = 0; i < 16; ++i) v[i] = (e0 + i < n) ? p[i] : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
+        }
+        store16<OUT_BF16, OUT_F32>(acc, e0, n, out_bf16, out_f32);
+    }
+}
+
+template <int FMT, bool B, bool F, bool SUM>
+static fp8q_status_t launch_reduce_t(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
+    static int resident = resident_blocks(dequant_reduce_kernel<FMT, B, F, SUM>, kRedThreads);
+    const size_t units = (n + 15) / 16;
+    const unsigned grid = grid_for((units + kRedThreads - 1) / kRedThreads, resident);
+    dequant_reduce_kernel<FMT, B, F, SUM><<<grid, kRedThreads, 0, s>>>(sh, k, n, ob, of);
+    return launch_status();
+}
+
+template <int FMT, bool SUM>
+static fp8q_status_t launch_reduce(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
+    if (ob && of) return launch_reduce_t<FMT, true, true, SUM>(sh, k, n, ob, of, s);
+    if (ob) return launch_reduce_t<FMT, true, false, SUM>(sh, k, n, ob, of, s);
+    return launch_reduce_t<FMT, false, true, SUM>(sh, k, n, ob, of, s);
+}
+
+template <bool B, bool F>
+static fp8q_status_t launch_sum_t(const float* ws, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
+    static int resident = resident_blocks(sum_f32_kernel<B, F>, kRedThreads);
+    const size_t units = (n + 15) / 16;
+    const unsigned grid = grid_for((units + kRedThreads - 1) / kRedThreads, resident);
+    sum_f32_kernel<B, F><<<grid, kRedThreads, 0, s>>>(ws, k, n, ob, of);
+    return launch_status();
+}
+
+// Shared argument checks of the multi-shard entry points.
+static fp8q_status_t check_shards(const uint8_t* const* codes, const float* const* scales, int k, size_t n,
+                                  fp8q_format_t fmt, const void* out_bf16, const float* out_fp32, ShardPtrs* sh) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
+    if (k < 1 || k > FP8Q_MAX_SHARDS) return FP8Q_ERR_K;
+    if (n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
+    if (n == 0) return FP8Q_OK;
+    if (!codes || !scales) return FP8Q_ERR_NULL;
+    if (!out_bf16 && !out_fp32) return FP8Q_ERR_NULL;
+    const size_t nb = fp8q_num_scales(n);
+    for (int r = 0; r < FP8Q_MAX_SHARDS; ++r) {
+        sh->codes[r] = nullptr;
+        sh->scales[r] = nullptr;
+    }
+    for (int r = 0; r < k; ++r) {
+        if (!codes[r] || !scales[r]) return FP8Q_ERR_NULL;
+        if (!aligned16(codes[r]) || !aligned16(scales[r])) return FP8Q_ERR_ALIGN;
+        if (overlaps(out_bf16, 2 * n, codes[r], n) || overlaps(out_bf16, 2 * n, scales[r], 4 * nb) ||
+            overlaps(out_fp32, 4 * n, codes[r], n) || overlaps(out_fp32, 4 * n, scales[r], 4 * nb))
+            return FP8Q_ERR_ALIAS;
+        sh->codes[r] = codes[r];
+        sh->scales[r] = scales[r];
+    }
+    if ((out_bf16 && !aligned16(out_bf16)) || (out_fp32 && !aligned16(out_fp32))) return FP8Q_ERR_ALIGN;
+    if (overlaps(out_bf16, 2 * n, out_fp32, 4 * n)) return FP8Q_ERR_ALIAS;
+    return FP8Q_OK;
+}
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" fp8q_status_t fp8q_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k,
+                                             size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
+                                             fp8q_stream_t stream) {
+    ShardPtrs sh;
+    fp8q_status_t st = check_shards(codes, scales, k, n, fmt, out_bf16, out_fp32, &sh);
+    if (st != FP8Q_OK || n == 0) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t* ob = static_cast<uint16_t*>(out_bf16);
+    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, true>(sh, k, n, ob, out_fp32, s)
+                            : launch_reduce<kE5M2, true>(sh, k, n, ob, out_fp32, s);
+}
+
+extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                                         void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
+    ShardPtrs sh;
+    const uint8_t* c[1] = {codes};
+    const float* sc[1] = {scales};
+    fp8q_status_t st = check_shards(c, sc, 1, n, fmt, out_bf16, out_fp32, &sh);
+    if (st != FP8Q_OK || n == 0) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t* ob = static_cast<uint16_t*>(out_bf16);
+    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(sh, 1, n, ob, out_fp32, s)
+                            : launch_reduce<kE5M2, false>(sh, 1, n, ob, out_fp32, s);
+}
+
+extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const float* const* scales,
+                                                     int k, size_t n, fp8q_format_t fmt, float* workspace,
+                                                     void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
+    ShardPtrs sh;
+    fp8q_status_t st = check_shards(codes, scales, k, n, fmt, out_bf16, out_fp32, &sh);
+    if (st != FP8Q_OK || n == 0) return st;
+    if (!workspace) return FP8Q_ERR_NULL;
+    if (!aligned16(workspace)) return FP8Q_ERR_ALIGN;
+    const size_t wbytes = 4 * (size_t)k * n;
+    if (overlaps(workspace, wbytes, out_bf16, 2 * n) || overlaps(workspace, wbytes, out_fp32, 4 * n))
+        return FP8Q_ERR_ALIAS;
+    for (int r = 0; r < k; ++r)
+        if (overlaps(workspace, wbytes, codes[r], n) || overlaps(workspace, wbytes, scales[r], 4 * fp8q_num_scales(n)))
+            return FP8Q_ERR_ALIAS;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int r = 0; r < k; ++r) {
+        ShardPtrs one;
+        one.codes[0] = sh.codes[r];
+        one.scales[0] = sh.scales[r];
+        st = fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(one, 1, n, nullptr, workspace + (size_t)r * n, s)
+                              : launch_reduce<kE5M2, false>(one, 1, n, nullptr, workspace + (size_t)r * n, s);
+        if (st != FP8Q_OK) return st;
+    }
+    uint16_t* ob = static_cast<uint16_t*>(out_bf16);
+    if (ob && out_fp32) return launch_sum_t<true, true>(workspace, k, n, ob, out_fp32, s);
+    if (ob) return launch_sum_t<true, false>(workspace, k, n, ob, out_fp32, s);
+    return launch_sum_t<false, true>(workspace, k, n, ob, out_fp32, s);
+}
