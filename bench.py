@@ -191,8 +191,8 @@ class Workload:
         self.n, self.k = n, k
         # the bucket of all 8 ranks in one allocation: shard r = rows r
         host = torch.empty((k, n), dtype=torch.bfloat16, pin_memory=True)
-        for r in range(k):
-            host[r].copy_(gen.ddp_shard(r + 8 * rank))
+        for r, seed in enumerate(rank_data_seeds(rank, k)):
+            host[r].copy_(gen.ddp_shard(seed))
         self.h_bucket = host
         self.bucket = host.to(dev)
         self.h_layer = []
@@ -387,6 +387,95 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- ranks ----
+def combine_over_ranks(dist, device, ms_local, bytes_local, elems_local):
+    """Whole-job figures: the slowest rank's step time, and the bytes and
+    elements of all ranks (each rank processes its own data).  `dist` is
+    torch.distributed with an initialised group, or None for one process."""
+    if dist is None:
+        return ms_local, bytes_local, elems_local
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([bytes_local, elems_local], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t[0].item()), float(u[0].item()), float(u[1].item())
+
+
+def rank_data_seeds(rank, k=8):
+    """Seeds of the bucket shards a rank works on: rank r takes 8r .. 8r+7,
+    so no two ranks quantize the same bytes."""
+    return [r + k * rank for r in range(k)]
+
+
+# -------------------------------------------------------- profile cases ----
+# kernel kind and index of its first launch in Workload.launches
+PROFILE_CASES = {"quantize": ("quantize_blockwise_kernel", 0), "reduce": ("dequant_reduce_kernel", 2),
+                 "ring_hop": ("ring_hop_kernel", 4), "mxfp8": ("mxfp8_quantize_kernel", 11)}
+
+
+def run_profile_case(case, launches):
+    """One kernel of the bench step, launched `launches` times on the bench's
+    own inputs (the inputs of each step kernel, prepared once), then exit."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = Workload(dev, 0, torch)
+    kind, first = PROFILE_CASES[case]
+    wl.run()                                   # every kernel's inputs exist
+    torch.cuda.synchronize()
+    _, nbytes, _, fn, fargs = wl.launches[first]
+    assert wl.launches[first][0] == kind
+    for _ in range(max(1, launches)):
+        st = fn(*fargs)
+        if st != 0:
+            raise RuntimeError(f"{case}: status {st}")
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": case, "kernel": kind, "launches": launches, "bytes_per_launch": nbytes}))
+
+
+def fused_vs_naive(wl, torch, reps=20):
+    """Time the fused 8-way reduce against the naive order (dequantize each
+    shard to fp32 in HBM, then sum) on the bench's e4m3 codes."""
+    L, n, k = wl.L, wl.n, wl.k
+    vp = ctypes.c_void_p
+    c, sc = wl.q[0]
+    cp = (vp * k)(*[c[r].data_ptr() for r in range(k)])
+    sp = (vp * k)(*[sc[r].data_ptr() for r in range(k)])
+    stride = int(L.fp8q_unfused_stride(n))
+    ws = torch.empty(k * stride, dtype=torch.float32, device=wl.dev)
+    ob, of = wl.red[0]
+    s = vp(wl.stream.cuda_stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=wl.dev)
+
+    def fused():
+        return L.fp8q_dequant_reduce(cp, sp, k, n, 0, vp(ob.data_ptr()), vp(of.data_ptr()), s)
+
+    def naive():
+        return L.fp8q_dequant_reduce_unfused(cp, sp, k, n, 0, vp(ws.data_ptr()), vp(ob.data_ptr()),
+                                             vp(of.data_ptr()), s)
+    out = {}
+    for name, fn in (("fused", fused), ("naive", naive)):
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for _ in range(reps):
+            flush.fill_(3)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(wl.stream)
+            if fn() != 0:
+                raise RuntimeError(f"{name} reduce failed")
+            b.record(wl.stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        out[name + "_us"] = round(1e3 * tot / reps, 2)
+    out["fused_over_naive"] = round(out["naive_us"] / out["fused_us"], 2)
+    out["naive_bytes"] = k * (n + 4 * nscales(n)) + 2 * k * 4 * n + n * 6
+    out["fused_bytes"] = bytes_reduce(n, k)
+    del ws
+    return out
+
+
 # ---------------------------------------------------------------- main ----
 def main():
     ap = argparse.ArgumentParser()
@@ -396,7 +485,13 @@ def main():
     ap.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                    help="launch one kernel of the step a few times on its bench inputs and exit (for ncu)")
+    ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.profile_launches)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -416,20 +511,6 @@ def main():
     def barrier():
         if world > 1:
             dist.barrier()
-
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    def sum_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
 
     wl = Workload(dev, rank, torch)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -474,9 +555,8 @@ def main():
             d["ms"] += dt
             d["bytes"] += nbytes
             d["elems"] += elems
-    ms_step = max_over_ranks(ms_local)
-    bytes_all = sum_over_ranks(float(wl.step_bytes))
-    elems_all = sum_over_ranks(float(wl.step_elems))
+    ms_step, bytes_all, elems_all = combine_over_ranks(dist if world > 1 else None, dev, ms_local,
+                                                       float(wl.step_bytes), float(wl.step_elems))
     value_gbs = bytes_all / (ms_step * 1e-3) / 1e9
 
     # ---------------- end to end: host buffers through the C ABI -----------
@@ -499,9 +579,11 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clocks.stop()
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps)
+    e2e_ms, _, _ = combine_over_ranks(dist if world > 1 else None, dev,
+                                      sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps, 0.0, 0.0)
     e2e_gbs = bytes_all / (e2e_ms * 1e-3) / 1e9
 
+    fvn = fused_vs_naive(wl, torch)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -537,6 +619,7 @@ def main():
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps},
         "gpu_launches": nl * steps,
+        "fused_vs_naive_reduce": fvn,
         "clocks": clock_info,
         "cpu_baseline": None,
     }

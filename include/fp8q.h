@@ -156,8 +156,13 @@ fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t 
 
 /* The naive order that (b) replaces ([P1]: "naive dequantize-then-reduce"),
  * kept as a comparator: each shard is dequantized to fp32 in `workspace`
- * (k * n floats, caller-owned), then the k fp32 arrays are summed in rank
- * order.  Bit-identical to fp8q_dequant_reduce; it only moves more bytes. */
+ * (caller-owned, k * fp8q_unfused_stride(n) floats; shard r's slot starts at
+ * float r * fp8q_unfused_stride(n)), then the k fp32 arrays are summed in
+ * rank order.  Bit-identical to fp8q_dequant_reduce; it only moves more bytes. */
+/* n rounded up to a multiple of 4: the per-shard fp32 slot of the workspace
+ * of fp8q_dequant_reduce_unfused, which keeps every slot 16-byte aligned. */
+size_t fp8q_unfused_stride(size_t n);
+
 fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const float* const* scales,
                                           int k, size_t n, fp8q_format_t fmt, float* workspace,
                                           void* out_bf16, float* out_fp32, fp8q_stream_t stream);

@@ -30,3 +30,13 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+def build_lib():
+    """Build libfp8q.so if needed (loads the build script by path, since
+    importing the package requires the built library)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("_fp8q_build", os.path.join(ROOT, "weight_transfer_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()

@@ -12,7 +12,7 @@ import re
 
 import pytest
 
-from conftest import ROOT
+from conftest import ROOT, build_lib
 
 OK, ERR_NULL, ERR_SIZE, ERR_ALIGN, ERR_FORMAT, ERR_K, ERR_CUDA, ERR_ALIAS = range(8)
 A = 0x7F0000000000            # a 16-byte aligned fake device address
@@ -21,8 +21,7 @@ MB = 1 << 20
 
 @pytest.fixture(scope="module")
 def L():
-    from weight_transfer_gb300 import build
-    build.build()
+    build_lib()
     import weight_transfer_gb300 as w
     return w.lib()
 

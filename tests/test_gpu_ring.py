@@ -66,8 +66,9 @@ def run_chain_gpu(w, parts, fmt):
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
-@pytest.mark.parametrize("payload", [1 << 10, 1 << 12, 1 << 16, 767 * 1024, 1 << 22, 1 << 24])
+@pytest.mark.parametrize("payload", [1 << p for p in range(10, 25)] + [767 * 1024])
 def test_ring_chain_full_check(w, orc, fmt, payload):
+    # per-hop payloads 1 KiB .. 16 MiB and 767 KiB, every element checked
     n = payload // 2
     host = [gen.ring_partial(r, n) for r in range(gen.RING_PARTIALS)]
     hops, last = run_chain_gpu(w, [p.cuda() for p in host], fmt)
@@ -80,9 +81,9 @@ def test_ring_chain_full_check(w, orc, fmt, payload):
     assert_same(bits16(last), b, "final bf16")
 
 
-@pytest.mark.parametrize("payload", [1 << 26, 1 << 28])
+@pytest.mark.parametrize("payload", [1 << 25, 1 << 26, 1 << 27, 1 << 28])
 def test_ring_chain_large_sampled(w, orc, payload):
-    # 64 MiB and 256 MiB per-hop payloads, checked on sampled 128-blocks:
+    # 32 MiB .. 256 MiB per-hop payloads, checked on sampled 128-blocks:
     # every hop is block-local, so the oracle replays the chain of a block
     # from that block's slice of the 8 partials
     n = payload // 2

@@ -8,7 +8,7 @@ library's CUDA kernels; there is no CPU path.  Outputs may be passed in
 (reused, caller-owned buffers) or are allocated with torch when omitted.
 
 Importing the package loads the library and fails loudly if it has not been
-built (``python -m weight_transfer_gb300.build`` or ``__graft_entry__.build()``).
+built (``python weight_transfer_gb300/build.py`` or ``__graft_entry__.build()``).
 """
 from __future__ import annotations
 
@@ -57,6 +57,7 @@ _SIGNATURES = {
     "fp8q_last_cuda_error": ([], _int),
     "fp8q_encode_f32": ([_vp, _sz, _int, _vp, _vp], _int),
     "fp8q_dequantize": ([_vp, _vp, _sz, _int, _vp, _vp, _vp], _int),
+    "fp8q_unfused_stride": ([_sz], _sz),
     "fp8q_dequant_reduce_unfused": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, _vp, _vp],
                                     _int),
 }
@@ -69,7 +70,7 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise ImportError(f"{LIB_PATH} is missing: build it with `python -m weight_transfer_gb300.build`; "
+            raise ImportError(f"{LIB_PATH} is missing: build it with `python weight_transfer_gb300/build.py`; "
                               "this package has no CPU fallback")
         L = ctypes.CDLL(LIB_PATH)
         for name, (args, res) in _SIGNATURES.items():
@@ -243,20 +244,22 @@ def fp8q_dequant_reduce_unfused(codes: Sequence[torch.Tensor], scales: Sequence[
                                 workspace: Optional[torch.Tensor] = None, out_bf16: Optional[torch.Tensor] = None,
                                 out_fp32: Optional[torch.Tensor] = None, want_bf16: bool = True,
                                 want_fp32: bool = True, n: Optional[int] = None, stream=None):
-    """The naive dequantize-to-HBM-then-reduce order (comparator); needs a k*n fp32 workspace."""
+    """The naive dequantize-to-HBM-then-reduce order (comparator); needs a
+    k * fp8q_unfused_stride(n) fp32 workspace."""
     k = len(codes)
     if n is None:
         n = codes[0].numel()
     dev = codes[0].device
+    stride = int(lib().fp8q_unfused_stride(n))
     if workspace is None:
-        workspace = torch.empty(k * n, dtype=torch.float32, device=dev)
+        workspace = torch.empty(max(k * stride, 1), dtype=torch.float32, device=dev)
     if out_bf16 is None and want_bf16:
         out_bf16 = torch.empty(n, dtype=torch.bfloat16, device=dev)
     if out_fp32 is None and want_fp32:
         out_fp32 = torch.empty(n, dtype=torch.float32, device=dev)
     cp = _ptr_array(codes, "codes", torch.uint8, n)
     sp = _ptr_array(scales, "scales", torch.float32, fp8q_num_scales(n))
-    st = lib().fp8q_dequant_reduce_unfused(cp, sp, k, n, _fmt(fmt), _dev(workspace, "workspace", torch.float32, k * n),
+    st = lib().fp8q_dequant_reduce_unfused(cp, sp, k, n, _fmt(fmt), _dev(workspace, "workspace", torch.float32, k * stride),
                                            _dev(out_bf16, "out_bf16", torch.bfloat16, n),
                                            _dev(out_fp32, "out_fp32", torch.float32, n), _stream(stream))
     _check("fp8q_dequant_reduce_unfused", st)

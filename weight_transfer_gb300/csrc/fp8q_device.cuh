@@ -109,6 +109,12 @@ __device__ __forceinline__ uint4 ld_once(const void* p) {
     return r;
 }
 
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ float ld_stream_f32(const float* p) {
     float r;
     asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(r) : "l"(p));
@@ -139,6 +145,12 @@ __device__ __forceinline__ uint4 ld_u8x16_tail(const uint8_t* p, long long avail
         if (i < avail) w[i >> 2] |= (uint32_t)p[i] << ((i & 3) * 8);
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
+__device__ __forceinline__ uint2 ld_u8x8_tail(const uint8_t* p, long long avail) {
+    uint32_t w[2] = {0u, 0u};
+    for (int i = 0; i < 8; ++i)
+        if (i < avail) w[i >> 2] |= (uint32_t)p[i] << ((i & 3) * 8);
+    return make_uint2(w[0], w[1]);
+}
 __device__ __forceinline__ void st_u8_tail(uint8_t* p, const uint32_t* w, int nwords, long long avail) {
     for (int i = 0; i < nwords * 4; ++i)
         if (i < avail) p[i] = (uint8_t)(w[i >> 2] >> ((i & 3) * 8));
@@ -153,8 +165,8 @@ __device__ __forceinline__ void st_f32_tail(float* p, const float* f, int count,
 }
 
 // --------------------------------------------------------------- scale ----
-// The block scale s = RN(amax / Fmax) and the quotient RN(x / s), both true
-// IEEE binary32 divisions (the compiler's correctly rounded div.rn.f32).
+// The block scale s = RN(amax / Fmax): a true IEEE binary32 division (the
+// compiler's correctly rounded div.rn.f32), once per block.
 template <int FMT>
 __device__ __forceinline__ float block_scale(float amax) {
     return __fdiv_rn(amax, FmtMax<FMT>::value);
@@ -164,6 +176,54 @@ __device__ __forceinline__ float block_scale(float amax) {
 // elements are signed zeros and are passed through unchanged.
 __device__ __forceinline__ float scaled_quotient(float x, float s) {
     return s == 0.0f ? x : __fdiv_rn(x, s);
+}
+
+__device__ __forceinline__ float with_sign_of(float mag, float sgn) {
+    return __uint_as_float((__float_as_uint(mag) & 0x7FFFFFFFu) | (__float_as_uint(sgn) & 0x80000000u));
+}
+
+// RN(x_i / s) for all elements of one block, without a per-element division.
+//
+// With y = RN(1/s) computed once (rcp.rn, correctly rounded), each quotient
+// is q0 = RN(x*y) followed by CORRECTIONS Markstein steps
+//     r = RN(x - q*s)  (fma),   q = RN(q + r*y)  (fma)
+// (P. Markstein, IBM J. Res. Dev. 34(1), 1990; "IA-64 and Elementary
+// Functions", 2000).  The sign is taken from x so that x = -0 stays -0.
+//
+//  * CORRECTIONS = 1 is used for bf16 dividends.  It equals RN(x/s) for all
+//    2^30 pairs of a bf16 significand and a binary32 significand at unit
+//    scale (exhaustive check in tests/fastdiv/check.c).
+//  * CORRECTIONS = 2 is used for binary32 dividends.  One step leaves q
+//    within half an ulp plus a 2^-46-relative term of x/s, i.e. faithful;
+//    Markstein's theorem (y = RN(1/s), q faithful => RN(q + r*y) = RN(x/s))
+//    makes the second step exact.
+//
+// Every operation commutes with power-of-two scaling of x and s while all
+// intermediates are normal binary32.  That holds for every element whose
+// code can be non-zero (|x/s| >= 2^-20) as soon as s >= 2^-58: then
+// |x| >= 2^-78 and the residual r, a non-zero multiple of 2^(e_x - 47), is
+// at least 2^-125.  Elements with |x/s| < 2^-20 round to a signed-zero code
+// either way (the result stays far below the smallest FP8 subnormal, 2^-16).
+// Blocks with s < 2^-58 (amax < 448 * 2^-58 for e4m3) take the IEEE
+// division instead.
+template <int CORRECTIONS, int N>
+__device__ __forceinline__ void block_quotients(const float* x, float s, float* q) {
+    if (s >= 0x1p-58f) {
+        const float y = __frcp_rn(s);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            float t = __fmul_rn(x[i], y);
+#pragma unroll
+            for (int c = 0; c < CORRECTIONS; ++c) {
+                const float r = __fmaf_rn(-t, s, x[i]);
+                t = __fmaf_rn(r, y, t);
+            }
+            q[i] = with_sign_of(t, x[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) q[i] = scaled_quotient(x[i], s);
+    }
 }
 
 }  // namespace fp8q

@@ -5,19 +5,21 @@
 // one fp32 scale per 128-element block, scale = amax / Fmax, codes are the
 // satfinite round-to-nearest-even conversion of x / scale.
 //
-// Work split: 16 lanes own one 128-element block (256 bytes of bf16, one
-// 16-byte load per lane); a warp covers two blocks per step and U steps are
-// loaded before any is processed, so each lane has U independent 16-byte
-// loads in flight.  The block amax is a 4-step xor-shuffle inside the
-// 16-lane group.  The grid is persistent (SM count x resident blocks) and
-// strides over warp-sized pairs of blocks.
+// Work split: 8 lanes own one 128-element block; lane j holds elements
+// [8j, 8j+8) and [64+8j, 64+8j+8), so each of the two 16-byte load
+// instructions of a warp reads four whole 128-byte half-blocks.  A warp covers
+// 4 blocks per step and U steps are loaded before any is processed (2U
+// independent 16-byte loads in flight per lane).  The block amax is a 3-step
+// xor-shuffle inside the 8-lane group; the quotients x / s use the per-block
+// reciprocal with one Markstein correction (exact for bf16 dividends, see
+// block_quotients).  The grid is persistent (SM count x resident blocks).
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
 namespace fp8q {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 4;
+constexpr int kQuantUnroll = 2;
 
 template <int FMT, int U>
 __global__ void __launch_bounds__(kQuantThreads)
@@ -25,43 +27,56 @@ quantize_blockwise_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __r
                           float* __restrict__ scales) {
     const size_t nb = (n + 127) >> 7;       // blocks, the last one possibly partial
     const size_t nfull = n >> 7;            // full blocks
-    const unsigned lane16 = threadIdx.x & 15u;
-    const unsigned half = (threadIdx.x >> 4) & 1u;
+    const unsigned lane = threadIdx.x & 31u;
+    const unsigned j = lane & 7u;           // lane inside the block's 8-lane group
+    const unsigned sub = lane >> 3;         // which of the warp's 4 blocks
     const size_t warp = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
 
     // the loop bound is warp-uniform so every shuffle below has all 32 lanes
-    for (size_t base = warp; 2 * base < nb; base += nwarps * U) {
-        uint4 v[U];
+    for (size_t base = warp; 4 * base < nb; base += nwarps * U) {
+        uint4 va[U], vb[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t b = 2 * (base + (size_t)u * nwarps) + half;
-            const size_t e0 = (b << 7) + lane16 * 8;
-            if (b < nfull) v[u] = ld_stream(x + e0);
-            else if (b < nb) v[u] = ld_bf16x8_tail(x + e0, (long long)n - (long long)e0);
-            else v[u] = make_uint4(0u, 0u, 0u, 0u);
+            const size_t b = 4 * (base + (size_t)u * nwarps) + sub;
+            const size_t e0 = (b << 7) + 8 * j;
+            if (b < nfull) {
+                va[u] = ld_stream(x + e0);
+                vb[u] = ld_stream(x + e0 + 64);
+            } else if (b < nb) {
+                va[u] = ld_bf16x8_tail(x + e0, (long long)n - (long long)e0);
+                vb[u] = ld_bf16x8_tail(x + e0 + 64, (long long)n - (long long)e0 - 64);
+            } else {
+                va[u] = make_uint4(0u, 0u, 0u, 0u);
+                vb[u] = va[u];
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const size_t b = 2 * (base + (size_t)u * nwarps) + half;
-            const size_t e0 = (b << 7) + lane16 * 8;
-            float f[8];
-            unpack8(v[u], f);
+            const size_t b = 4 * (base + (size_t)u * nwarps) + sub;
+            const size_t e0 = (b << 7) + 8 * j;
+            float f[16];
+            unpack8(va[u], *reinterpret_cast<float(*)[8]>(f));
+            unpack8(vb[u], *reinterpret_cast<float(*)[8]>(f + 8));
             float a = fabsf(f[0]);
 #pragma unroll
-            for (int i = 1; i < 8; ++i) a = fmaxf(a, fabsf(f[i]));
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
+            for (int i = 1; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
             a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
             a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
             a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
             const float s = block_scale<FMT>(a);
-            float q[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = scaled_quotient(f[i], s);
-            uint32_t w[2] = {cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])};
-            if (b < nfull) st_stream(codes + e0, make_uint2(w[0], w[1]));
-            else if (b < nb) st_u8_tail(codes + e0, w, 2, (long long)n - (long long)e0);
-            if (b < nb && lane16 == 0) scales[b] = s;
+            float q[16];
+            block_quotients<1, 16>(f, s, q);
+            uint32_t wa[2] = {cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])};
+            uint32_t wb[2] = {cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]), cvt_fp8x4<FMT>(q[12], q[13], q[14], q[15])};
+            if (b < nfull) {
+                st_stream(codes + e0, make_uint2(wa[0], wa[1]));
+                st_stream(codes + e0 + 64, make_uint2(wb[0], wb[1]));
+            } else if (b < nb) {
+                st_u8_tail(codes + e0, wa, 2, (long long)n - (long long)e0);
+                st_u8_tail(codes + e0 + 64, wb, 2, (long long)n - (long long)e0 - 64);
+            }
+            if (b < nb && j == 0) scales[b] = s;
         }
     }
 }
@@ -90,7 +105,7 @@ static fp8q_status_t launch_quantize(const uint16_t* x, size_t n, uint8_t* codes
                                      cudaStream_t stream) {
     static int resident = resident_blocks(quantize_blockwise_kernel<FMT, kQuantUnroll>, kQuantThreads);
     const size_t nb = (n + 127) / 128;
-    const size_t blocks_per_cta = (kQuantThreads / 16) * kQuantUnroll;
+    const size_t blocks_per_cta = (kQuantThreads / 8) * kQuantUnroll;
     const unsigned grid = grid_for((nb + blocks_per_cta - 1) / blocks_per_cta, resident);
     quantize_blockwise_kernel<FMT, kQuantUnroll><<<grid, kQuantThreads, 0, stream>>>(x, n, codes, scales);
     return launch_status();

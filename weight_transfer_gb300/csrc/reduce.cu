@@ -95,11 +95,11 @@ dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_
     }
 }
 
-// Second pass of the naive order: k fp32 arrays (stride n apart) summed in
-// rank order from +0.
+// Second pass of the naive order: k fp32 arrays (`slot` floats apart, a
+// multiple of 4 so every slot is 16-byte aligned) summed in rank order from +0.
 template <bool OUT_BF16, bool OUT_F32>
 __global__ void __launch_bounds__(kRedThreads)
-sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, uint16_t* __restrict__ out_bf16,
+sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, size_t slot, uint16_t* __restrict__ out_bf16,
                float* __restrict__ out_f32) {
     const size_t units = (n + 15) >> 4;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -110,9 +110,9 @@ sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, uint16_t* __restri
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
         for (int r = 0; r < k; ++r) {
-            const float* p = ws + (size_t)r * n + e0;
+            const float* p = ws + (size_t)r * slot + e0;
             float v[16];
-            if (full && ((reinterpret_cast<uintptr_t>(p) & 15u) == 0)) {
+            if (full) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint4 t = ld_stream(p + 4 * q);
@@ -146,11 +146,12 @@ static fp8q_status_t launch_reduce(const ShardPtrs& sh, int k, size_t n, uint16_
 }
 
 template <bool B, bool F>
-static fp8q_status_t launch_sum_t(const float* ws, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
+static fp8q_status_t launch_sum_t(const float* ws, int k, size_t n, size_t stride, uint16_t* ob, float* of,
+                                  cudaStream_t s) {
     static int resident = resident_blocks(sum_f32_kernel<B, F>, kRedThreads);
     const size_t units = (n + 15) / 16;
     const unsigned grid = grid_for((units + kRedThreads - 1) / kRedThreads, resident);
-    sum_f32_kernel<B, F><<<grid, kRedThreads, 0, s>>>(ws, k, n, ob, of);
+    sum_f32_kernel<B, F><<<grid, kRedThreads, 0, s>>>(ws, k, n, stride, ob, of);
     return launch_status();
 }
 
@@ -186,6 +187,8 @@ static fp8q_status_t check_shards(const uint8_t* const* codes, const float* cons
 
 using namespace fp8q;
 
+extern "C" size_t fp8q_unfused_stride(size_t n) { return (n + 3) & ~(size_t)3; }
+
 extern "C" fp8q_status_t fp8q_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k,
                                              size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
                                              fp8q_stream_t stream) {
@@ -219,7 +222,8 @@ extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes
     if (st != FP8Q_OK || n == 0) return st;
     if (!workspace) return FP8Q_ERR_NULL;
     if (!aligned16(workspace)) return FP8Q_ERR_ALIGN;
-    const size_t wbytes = 4 * (size_t)k * n;
+    const size_t stride = fp8q_unfused_stride(n);      // keeps every shard slot 16-byte aligned
+    const size_t wbytes = 4 * (size_t)k * stride;
     if (overlaps(workspace, wbytes, out_bf16, 2 * n) || overlaps(workspace, wbytes, out_fp32, 4 * n))
         return FP8Q_ERR_ALIAS;
     for (int r = 0; r < k; ++r)
@@ -230,12 +234,12 @@ extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes
         ShardPtrs one;
         one.codes[0] = sh.codes[r];
         one.scales[0] = sh.scales[r];
-        st = fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(one, 1, n, nullptr, workspace + (size_t)r * n, s)
-                              : launch_reduce<kE5M2, false>(one, 1, n, nullptr, workspace + (size_t)r * n, s);
+        st = fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(one, 1, n, nullptr, workspace + (size_t)r * stride, s)
+                              : launch_reduce<kE5M2, false>(one, 1, n, nullptr, workspace + (size_t)r * stride, s);
         if (st != FP8Q_OK) return st;
     }
     uint16_t* ob = static_cast<uint16_t*>(out_bf16);
-    if (ob && out_fp32) return launch_sum_t<true, true>(workspace, k, n, ob, out_fp32, s);
-    if (ob) return launch_sum_t<true, false>(workspace, k, n, ob, out_fp32, s);
-    return launch_sum_t<false, true>(workspace, k, n, ob, out_fp32, s);
+    if (ob && out_fp32) return launch_sum_t<true, true>(workspace, k, n, stride, ob, out_fp32, s);
+    if (ob) return launch_sum_t<true, false>(workspace, k, n, stride, ob, out_fp32, s);
+    return launch_sum_t<false, true>(workspace, k, n, stride, ob, out_fp32, s);
 }

@@ -8,9 +8,13 @@
 // the next hop, in one pass: the sums stay in registers while the block amax
 // is reduced, nothing is re-read from HBM.
 //
-// Work split: a lane owns 16 consecutive elements (16 bytes of codes, 32
-// bytes of the local partial), 8 lanes cover one 128-element block and the
-// amax is a 3-step xor-shuffle among them; a warp covers 4 blocks per step.
+// Work split: 8 lanes own one 128-element block; lane j holds elements
+// [8j, 8j+8) and [64+8j, 64+8j+8) (two 16-byte loads of the local partial,
+// two 8-byte loads of codes), so every load instruction of a warp reads whole
+// 128-byte (bf16) or 64-byte (codes) half-blocks.  The amax is a 3-step
+// xor-shuffle among the 8 lanes; a warp covers 4 blocks per step.  The
+// quotients y / s use the per-block reciprocal with two Markstein
+// corrections (exact for binary32 dividends, see block_quotients).
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
@@ -23,36 +27,40 @@ __global__ void __launch_bounds__(kHopThreads)
 ring_hop_kernel(const uint8_t* __restrict__ in_codes, const float* __restrict__ in_scales,
                 const uint16_t* local, size_t n, uint8_t* __restrict__ out_codes,
                 float* __restrict__ out_scales, uint16_t* out_bf16) {
-    const size_t units = (n + 15) >> 4;
+    const size_t nb = (n + 127) >> 7;
+    const size_t nfull = n >> 7;
     const unsigned lane = threadIdx.x & 31u;
+    const unsigned j = lane & 7u;
+    const unsigned sub = lane >> 3;
     const size_t warp = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
-    for (size_t base = warp; base * 32 < units; base += nwarps) {    // warp-uniform bound
-        const size_t u = base * 32 + lane;
-        const size_t e0 = u << 4;
-        const size_t b = u >> 3;
-        const long long avail = (long long)n - (long long)e0;
-        const bool full = avail >= 16;
-        uint4 c = make_uint4(0u, 0u, 0u, 0u), l0 = c, l1 = c;
+    for (size_t base = warp; 4 * base < nb; base += nwarps) {    // warp-uniform bound
+        const size_t b = 4 * base + sub;
+        const size_t e0 = (b << 7) + 8 * j;
+        const long long avail = (long long)n - (long long)e0;      // valid elements from e0
+        uint2 ca = make_uint2(0u, 0u), cb = ca;
+        uint4 la = make_uint4(0u, 0u, 0u, 0u), lb = la;
         float s_in = 0.0f;
-        if (full) {
-            c = ld_stream(in_codes + e0);
-            l0 = ld_once(local + e0);
-            l1 = ld_once(local + e0 + 8);
-        } else if (avail > 0) {
-            c = ld_u8x16_tail(in_codes + e0, avail);
-            l0 = ld_bf16x8_tail(local + e0, avail);
-            l1 = ld_bf16x8_tail(local + e0 + 8, avail - 8);
+        if (b < nfull) {
+            ca = ld_stream8(in_codes + e0);
+            cb = ld_stream8(in_codes + e0 + 64);
+            la = ld_once(local + e0);
+            lb = ld_once(local + e0 + 64);
+        } else if (b < nb) {
+            ca = ld_u8x8_tail(in_codes + e0, avail);
+            cb = ld_u8x8_tail(in_codes + e0 + 64, avail - 64);
+            la = ld_bf16x8_tail(local + e0, avail);
+            lb = ld_bf16x8_tail(local + e0 + 64, avail - 64);
         }
-        if (avail > 0) s_in = ld_stream_f32(in_scales + b);
+        if (b < nb) s_in = ld_stream_f32(in_scales + b);
 
         float d[16], lf[16], y[16];
-        decode_fp8x4<FMT>(c.x, d);
-        decode_fp8x4<FMT>(c.y, d + 4);
-        decode_fp8x4<FMT>(c.z, d + 8);
-        decode_fp8x4<FMT>(c.w, d + 12);
-        unpack8(l0, *reinterpret_cast<float(*)[8]>(lf));
-        unpack8(l1, *reinterpret_cast<float(*)[8]>(lf + 8));
+        decode_fp8x4<FMT>(ca.x, d);
+        decode_fp8x4<FMT>(ca.y, d + 4);
+        decode_fp8x4<FMT>(cb.x, d + 8);
+        decode_fp8x4<FMT>(cb.y, d + 12);
+        unpack8(la, *reinterpret_cast<float(*)[8]>(lf));
+        unpack8(lb, *reinterpret_cast<float(*)[8]>(lf + 8));
         float a = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -64,23 +72,30 @@ ring_hop_kernel(const uint8_t* __restrict__ in_codes, const float* __restrict__ 
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
         const float s = block_scale<FMT>(a);
         float q[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = scaled_quotient(y[i], s);
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w[j] = cvt_fp8x4<FMT>(q[4 * j], q[4 * j + 1], q[4 * j + 2], q[4 * j + 3]);
-        if (full) st_stream(out_codes + e0, make_uint4(w[0], w[1], w[2], w[3]));
-        else if (avail > 0) st_u8_tail(out_codes + e0, w, 4, avail);
-        if (avail > 0 && (lane & 7u) == 0) out_scales[b] = s;
+        block_quotients<2, 16>(y, s, q);
+        uint32_t wa[2] = {cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])};
+        uint32_t wb[2] = {cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]), cvt_fp8x4<FMT>(q[12], q[13], q[14], q[15])};
+        if (b < nfull) {
+            st_stream(out_codes + e0, make_uint2(wa[0], wa[1]));
+            st_stream(out_codes + e0 + 64, make_uint2(wb[0], wb[1]));
+        } else if (b < nb) {
+            st_u8_tail(out_codes + e0, wa, 2, avail);
+            st_u8_tail(out_codes + e0 + 64, wb, 2, avail - 64);
+        }
+        if (b < nb && j == 0) out_scales[b] = s;
         if (OUT_BF16) {
-            uint32_t h[8];
+            uint32_t ha[4], hb[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) h[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
-            if (full) {
-                st_stream(out_bf16 + e0, make_uint4(h[0], h[1], h[2], h[3]));
-                st_stream(out_bf16 + e0 + 8, make_uint4(h[4], h[5], h[6], h[7]));
-            } else if (avail > 0) {
-                st_u16_tail(out_bf16 + e0, h, 8, avail);
+            for (int i = 0; i < 4; ++i) {
+                ha[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
+                hb[i] = pack_bf16x2(y[8 + 2 * i], y[8 + 2 * i + 1]);
+            }
+            if (b < nfull) {
+                st_stream(out_bf16 + e0, make_uint4(ha[0], ha[1], ha[2], ha[3]));
+                st_stream(out_bf16 + e0 + 64, make_uint4(hb[0], hb[1], hb[2], hb[3]));
+            } else if (b < nb) {
+                st_u16_tail(out_bf16 + e0, ha, 4, avail);
+                st_u16_tail(out_bf16 + e0 + 64, hb, 4, avail - 64);
             }
         }
     }
@@ -90,8 +105,8 @@ template <int FMT, bool B>
 static fp8q_status_t launch_hop_t(const uint8_t* ic, const float* is, const uint16_t* loc, size_t n, uint8_t* oc,
                                   float* os, uint16_t* ob, cudaStream_t s) {
     static int resident = resident_blocks(ring_hop_kernel<FMT, B>, kHopThreads);
-    const size_t units = (n + 15) / 16;
-    const unsigned grid = grid_for((units + kHopThreads - 1) / kHopThreads, resident);
+    const size_t blocks_per_cta = (kHopThreads / 32) * 4;
+    const unsigned grid = grid_for(((n + 127) / 128 + blocks_per_cta - 1) / blocks_per_cta, resident);
     ring_hop_kernel<FMT, B><<<grid, kHopThreads, 0, s>>>(ic, is, loc, n, oc, os, ob);
     return launch_status();
 }
