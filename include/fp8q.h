@@ -167,6 +167,39 @@ fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const flo
                                           int k, size_t n, fp8q_format_t fmt, float* workspace,
                                           void* out_bf16, float* out_fp32, fp8q_stream_t stream);
 
+/* ----------------------------------------------- no-allocation variant ----
+ * Not a step of the codec (the source pages have no counterpart): the
+ * unfused comparator above with its scratch inside the library instead of
+ * a caller-supplied workspace.
+ *
+ * Who needs it: callers that cannot call cudaMalloc.  An interception layer
+ * slotted under a training framework runs in a process whose device memory
+ * belongs to the framework's caching allocator, and it has no handle to that
+ * allocator; and on a busy GPU a cudaMalloc / cudaFree pair can synchronize
+ * the device and stall every stream.  Such a caller still passes its inputs
+ * and outputs, but no workspace.
+ *
+ * The scratch is one static device array of FP8Q_STATIC_SCRATCH_FLOATS
+ * floats (16 MiB) in the library, reserved on every GPU that loads the
+ * library until the process exits.  Each shard uses fp8q_unfused_stride(n)
+ * floats of it, so the call needs k * fp8q_unfused_stride(n) <=
+ * FP8Q_STATIC_SCRATCH_FLOATS; larger calls return FP8Q_ERR_SIZE and launch
+ * nothing.  The call allocates nothing: no cudaMalloc, no cudaFree.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and keeps it; make that first call before any stream
+ * capture.  All calls share the one array and it keeps whatever the last
+ * call left there; nothing in it needs clearing, because every call writes
+ * each scratch element it reads before reading it.  Calls whose work
+ * overlaps on the GPU (different streams, or concurrent host threads) race
+ * on the array: order them on one stream or with events.
+ * Arguments and results are otherwise those of fp8q_dequant_reduce_unfused. */
+#define FP8Q_STATIC_SCRATCH_FLOATS (1u << 22)
+
+fp8q_status_t fp8q_dequant_reduce_unfused_static(const uint8_t* const* codes, const float* const* scales,
+                                                 int k, size_t n, fp8q_format_t fmt, void* out_bf16,
+                                                 float* out_fp32, fp8q_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

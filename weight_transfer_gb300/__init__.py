@@ -58,6 +58,8 @@ _SIGNATURES = {
     "fp8q_encode_f32": ([_vp, _sz, _int, _vp, _vp], _int),
     "fp8q_dequantize": ([_vp, _vp, _sz, _int, _vp, _vp, _vp], _int),
     "fp8q_unfused_stride": ([_sz], _sz),
+    "fp8q_dequant_reduce_unfused_static": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, _vp],
+                                           _int),
     "fp8q_dequant_reduce_unfused": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, _vp, _vp],
                                     _int),
 }
@@ -263,4 +265,32 @@ def fp8q_dequant_reduce_unfused(codes: Sequence[torch.Tensor], scales: Sequence[
                                            _dev(out_bf16, "out_bf16", torch.bfloat16, n),
                                            _dev(out_fp32, "out_fp32", torch.float32, n), _stream(stream))
     _check("fp8q_dequant_reduce_unfused", st)
+    return out_bf16, out_fp32
+
+
+FP8Q_STATIC_SCRATCH_FLOATS = 1 << 22
+
+
+def fp8q_dequant_reduce_unfused_static(codes: Sequence[torch.Tensor], scales: Sequence[torch.Tensor], fmt="e4m3",
+                                       out_bf16: Optional[torch.Tensor] = None,
+                                       out_fp32: Optional[torch.Tensor] = None, want_bf16: bool = True,
+                                       want_fp32: bool = True, n: Optional[int] = None, stream=None):
+    """The unfused comparator with the library's static scratch instead of a
+    workspace, for callers that cannot allocate device memory.  Requires
+    k * fp8q_unfused_stride(n) <= FP8Q_STATIC_SCRATCH_FLOATS; calls that
+    overlap on the GPU race on the shared scratch."""
+    k = len(codes)
+    if n is None:
+        n = codes[0].numel()
+    dev = codes[0].device
+    if out_bf16 is None and want_bf16:
+        out_bf16 = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    if out_fp32 is None and want_fp32:
+        out_fp32 = torch.empty(n, dtype=torch.float32, device=dev)
+    cp = _ptr_array(codes, "codes", torch.uint8, n)
+    sp = _ptr_array(scales, "scales", torch.float32, fp8q_num_scales(n))
+    st = lib().fp8q_dequant_reduce_unfused_static(cp, sp, k, n, _fmt(fmt),
+                                                  _dev(out_bf16, "out_bf16", torch.bfloat16, n),
+                                                  _dev(out_fp32, "out_fp32", torch.float32, n), _stream(stream))
+    _check("fp8q_dequant_reduce_unfused_static", st)
     return out_bf16, out_fp32

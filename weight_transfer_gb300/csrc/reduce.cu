@@ -12,6 +12,8 @@
 // in flight per lane), then the sum runs in rank order 0..k-1:
 //   acc = +0;  acc = RN(acc + RN(decode(c_r) * s_r))
 // with explicit _rn intrinsics so nothing is fused into an FMA.
+#include <mutex>
+
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
@@ -242,4 +244,63 @@ extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes
     if (ob && out_fp32) return launch_sum_t<true, true>(workspace, k, n, stride, ob, out_fp32, s);
     if (ob) return launch_sum_t<true, false>(workspace, k, n, stride, ob, out_fp32, s);
     return launch_sum_t<false, true>(workspace, k, n, stride, ob, out_fp32, s);
+}
+
+// ------------------------------------------------- no-allocation variant ----
+// fp8q_dequant_reduce_unfused with its workspace in a static device array
+// instead of a caller-supplied buffer (for callers that cannot allocate).
+
+namespace fp8q {
+
+static __device__ __align__(256) float g_static_scratch[FP8Q_STATIC_SCRATCH_FLOATS];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_static_scratch_mu;
+static float* g_static_scratch_ptr[kMaxDevices];
+
+// Device address of g_static_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and kept.
+static fp8q_status_t static_scratch_address(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_status(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_static_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_static_scratch_ptr[dev];
+    return FP8Q_OK;
+}
+
+}  // namespace fp8q
+
+extern "C" fp8q_status_t fp8q_dequant_reduce_unfused_static(const uint8_t* const* codes, const float* const* scales,
+                                                            int k, size_t n, fp8q_format_t fmt, void* out_bf16,
+                                                            float* out_fp32, fp8q_stream_t stream) {
+    ShardPtrs sh;
+    fp8q_status_t st = check_shards(codes, scales, k, n, fmt, out_bf16, out_fp32, &sh);
+    if (st != FP8Q_OK || n == 0) return st;
+    const size_t slot = fp8q_unfused_stride(n);
+    if (slot > FP8Q_STATIC_SCRATCH_FLOATS / (size_t)k) return FP8Q_ERR_SIZE;
+    float* ws = nullptr;
+    st = static_scratch_address(&ws);
+    if (st != FP8Q_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int r = 0; r < k; ++r) {
+        ShardPtrs one;
+        one.codes[0] = sh.codes[r];
+        one.scales[0] = sh.scales[r];
+        st = fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(one, 1, n, nullptr, ws + (size_t)r * slot, s)
+                              : launch_reduce<kE5M2, false>(one, 1, n, nullptr, ws + (size_t)r * slot, s);
+        if (st != FP8Q_OK) return st;
+    }
+    uint16_t* ob = static_cast<uint16_t*>(out_bf16);
+    if (ob && out_fp32) return launch_sum_t<true, true>(ws, k, n, slot, ob, out_fp32, s);
+    if (ob) return launch_sum_t<true, false>(ws, k, n, slot, ob, out_fp32, s);
+    return launch_sum_t<false, true>(ws, k, n, slot, ob, out_fp32, s);
 }
