@@ -177,51 +177,54 @@ def ncu_traffic(name):
     return None
 
 
-# ------------------------------------------------------------ workload ----
-class Workload:
-    """Inputs, preallocated outputs and the launch list of one step."""
+# ------------------------------------------------------------- L2 flush ----
+class L2Flush:
+    """Evicts L2 between timed steps: writes a buffer larger than L2, then
+    reads a second one, so that the written lines are back in HBM (and the L2
+    holds clean, unrelated lines) before the next step's events start."""
 
-    def __init__(self, dev, rank, torch):
-        import gen
-        import weight_transfer_gb300 as w
-        self.torch, self.w, self.dev = torch, w, dev
-        L = w.lib()
-        self.L = L
-        n, k = gen.DDP_N, gen.DDP_K
-        self.n, self.k = n, k
-        # the bucket of all 8 ranks in one allocation: shard r = rows r
-        host = torch.empty((k, n), dtype=torch.bfloat16, pin_memory=True)
-        for r, seed in enumerate(rank_data_seeds(rank, k)):
-            host[r].copy_(gen.ddp_shard(seed))
-        self.h_bucket = host
-        self.bucket = host.to(dev)
-        self.h_layer = []
-        self.layer = []
-        for t in range(len(gen.QWEN3_TENSORS)):
-            ht = gen.qwen3_tensor(rank, t).pin_memory()
-            self.h_layer.append(ht)
-            self.layer.append(ht.to(dev))
-        self.tensors = gen.QWEN3_TENSORS
+    def __init__(self, torch, dev, nbytes=L2_FLUSH_BYTES):
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(nbytes // 4, dtype=torch.float32, device=dev)
+        self.i = 0
+
+    def __call__(self):
+        self.i += 1
+        self.w.fill_(self.i & 0xFF)
+        self.r.sum()
+
+
+# ------------------------------------------------------------ workload ----
+class DeviceSet:
+    """One set of device buffers for a step (inputs and outputs) and the
+    step's launch list bound to them, arguments marshalled once so that a
+    launch costs one ctypes call."""
+
+    def __init__(self, wl, stream):
+        torch, dev, L, n, k = wl.torch, wl.dev, wl.L, wl.n, wl.k
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         nb = nscales(n)
+        self.stream = stream
+        self.bucket = torch.empty((k, n), dtype=bf, device=dev)
+        self.layer = [torch.empty(h.shape, dtype=bf, device=dev) for h in wl.h_layer]
         self.q = {f: (torch.empty((k, n), dtype=u8, device=dev), torch.empty((k, nb), dtype=f32, device=dev))
                   for f in (0, 1)}
         self.red = {f: (torch.empty(n, dtype=bf, device=dev), torch.empty(n, dtype=f32, device=dev)) for f in (0, 1)}
-        self.hops = [(torch.empty(n, dtype=u8, device=dev), torch.empty(nb, dtype=f32, device=dev)) for _ in range(k - 1)]
+        self.hops = [(torch.empty(n, dtype=u8, device=dev), torch.empty(nb, dtype=f32, device=dev))
+                     for _ in range(k - 1)]
         self.ring_bf16 = torch.empty(n, dtype=bf, device=dev)
         self.mx = []
-        for (name, b, m, kk) in self.tensors:
-            sb = w.mxfp8_swizzled_scale_bytes(b, m, kk)
+        for (name, b, m, kk) in wl.tensors:
+            sb = wl.w.mxfp8_swizzled_scale_bytes(b, m, kk)
             self.mx.append((torch.empty((b, m, kk), dtype=u8, device=dev), torch.empty(sb, dtype=u8, device=dev), sb))
-        self._build_launches()
+        # the results a caller reads back
+        self.outputs = [self.q[0][0], self.q[0][1], self.q[1][0], self.q[1][1], self.red[0][0], self.red[0][1],
+                        self.red[1][0], self.red[1][1], self.hops[-1][0], self.hops[-1][1], self.ring_bf16]
+        for c, sc, _ in self.mx:
+            self.outputs += [c, sc]
 
-    def _build_launches(self):
-        """(kernel, algorithmic bytes, elements, zero-arg callable) per launch;
-        arguments are marshalled once so a launch costs one ctypes call."""
-        L, n, k = self.L, self.n, self.k
         vp = ctypes.c_void_p
-        self.stream = self.torch.cuda.current_stream(self.dev)
-        s = vp(self.stream.cuda_stream)
+        sp_ = vp(stream.cuda_stream)
         launches = []
 
         def add(kind, nbytes, elems, fn, *args):
@@ -231,7 +234,7 @@ class Workload:
             c, sc = self.q[f]
             add("quantize_blockwise_kernel", bytes_quantize(k * n), k * n, L.fp8q_quantize_blockwise,
                 vp(self.bucket.data_ptr()), ctypes.c_size_t(k * n), ctypes.c_int(f), vp(c.data_ptr()),
-                vp(sc.data_ptr()), s)
+                vp(sc.data_ptr()), sp_)
         self._keep = []
         for f in (0, 1):
             c, sc = self.q[f]
@@ -240,25 +243,28 @@ class Workload:
             self._keep += [cp, sp]
             ob, of = self.red[f]
             add("dequant_reduce_kernel", bytes_reduce(n, k), n, L.fp8q_dequant_reduce, cp, sp, ctypes.c_int(k),
-                ctypes.c_size_t(n), ctypes.c_int(f), vp(ob.data_ptr()), vp(of.data_ptr()), s)
+                ctypes.c_size_t(n), ctypes.c_int(f), vp(ob.data_ptr()), vp(of.data_ptr()), sp_)
         prev = (self.q[0][0][0], self.q[0][1][0])        # hop 0 = e4m3 quantize of rank 0's shard
         for h in range(1, k):
             oc, osc = self.hops[h - 1]
             last = h == k - 1
             add("ring_hop_kernel", bytes_hop(n, last), n, L.fp8q_ring_hop, vp(prev[0].data_ptr()),
                 vp(prev[1].data_ptr()), vp(self.bucket[h].data_ptr()), ctypes.c_size_t(n), ctypes.c_int(0),
-                vp(oc.data_ptr()), vp(osc.data_ptr()), vp(self.ring_bf16.data_ptr() if last else None), s)
+                vp(oc.data_ptr()), vp(osc.data_ptr()), vp(self.ring_bf16.data_ptr() if last else None), sp_)
             prev = (oc, osc)
-        for (name, b, m, kk), x, (c, sc, sb) in zip(self.tensors, self.layer, self.mx):
-            add("mxfp8_quantize_kernel", bytes_mxfp8(b, m, kk, sb), b * m * kk, L.mxfp8_quantize_swizzled,
-                vp(x.data_ptr()), ctypes.c_int64(b), ctypes.c_int64(m), ctypes.c_int64(kk), vp(c.data_ptr()),
-                vp(sc.data_ptr()), s)
+        # the whole layer (expert batches and attention matrices) in one launch
+        self._group = (wl.w.mxfp8_tensor_t * len(wl.tensors))()
+        mx_bytes = mx_elems = 0
+        for i, ((name, b, m, kk), x, (c, sc, sb)) in enumerate(zip(wl.tensors, self.layer, self.mx)):
+            self._group[i] = wl.w.mxfp8_tensor_t(x.data_ptr(), b, m, kk, c.data_ptr(), sc.data_ptr())
+            mx_bytes += bytes_mxfp8(b, m, kk, sb)
+            mx_elems += b * m * kk
+        add("mxfp8_quantize_kernel", mx_bytes, mx_elems, L.mxfp8_quantize_swizzled_group, self._group,
+            ctypes.c_int(len(wl.tensors)), sp_)
         self.launches = launches
-        self.step_bytes = sum(l[1] for l in launches)
-        self.step_elems = sum(l[2] for l in launches)
 
     def run(self, events=None):
-        """Launch one step on the current stream; with `events`, bracket each
+        """Launch one step on this set's stream; with `events`, bracket each
         launch with a pair of timing events."""
         for i, (_, _, _, fn, args) in enumerate(self.launches):
             if events is not None:
@@ -269,27 +275,129 @@ class Workload:
             if events is not None:
                 events[2 * i + 1].record(self.stream)
 
-    def h2d(self):
-        self.bucket.copy_(self.h_bucket, non_blocking=True)
-        for d, h in zip(self.layer, self.h_layer):
-            d.copy_(h, non_blocking=True)
+
+class Workload:
+    """The step's inputs in pinned host memory and the device sets that run
+    it (one for the device-resident timing, two for the copy pipeline)."""
+
+    def __init__(self, dev, rank, torch):
+        import gen
+        import weight_transfer_gb300 as w
+        self.torch, self.w, self.dev = torch, w, dev
+        self.L = w.lib()
+        n, k = gen.DDP_N, gen.DDP_K
+        self.n, self.k = n, k
+        # the bucket of all 8 ranks in one allocation: shard r = rows r
+        host = torch.empty((k, n), dtype=torch.bfloat16, pin_memory=True)
+        for r, seed in enumerate(rank_data_seeds(rank, k)):
+            host[r].copy_(gen.ddp_shard(seed))
+        self.h_bucket = host
+        self.tensors = gen.QWEN3_TENSORS
+        self.h_layer = [gen.qwen3_tensor(rank, t).pin_memory() for t in range(len(self.tensors))]
+        self.stream = torch.cuda.current_stream(dev)
+        self.sets = [DeviceSet(self, self.stream)]
+        self.h2d(self.sets[0], self.stream)
+        torch.cuda.synchronize(dev)
+        self.launches = self.sets[0].launches
+        self.step_bytes = sum(l[1] for l in self.launches)
+        self.step_elems = sum(l[2] for l in self.launches)
+        self.h_out = None
+
+    # the main timed loop and the profile cases use set 0
+    @property
+    def q(self):
+        return self.sets[0].q
+
+    @property
+    def red(self):
+        return self.sets[0].red
+
+    def run(self, events=None):
+        self.sets[0].run(events)
+
+    def h2d(self, ds, stream):
+        """Copies the step's inputs from pinned host memory into set `ds`."""
+        with self.torch.cuda.stream(stream):
+            ds.bucket.copy_(self.h_bucket, non_blocking=True)
+            for d, h in zip(ds.layer, self.h_layer):
+                d.copy_(h, non_blocking=True)
         return self.h_bucket.numel() * 2 + sum(h.numel() * 2 for h in self.h_layer)
 
-    def alloc_host_outputs(self):
-        t = self.torch
-        outs = [self.q[0][0], self.q[0][1], self.q[1][0], self.q[1][1], self.red[0][0], self.red[0][1],
-                self.red[1][0], self.red[1][1], self.hops[-1][0], self.hops[-1][1], self.ring_bf16]
-        for c, sc, sb in self.mx:
-            outs += [c, sc]
-        self.d_outs = outs
-        self.h_outs = [t.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-
-    def d2h(self):
+    def d2h(self, ds, stream):
+        """Reads every result of set `ds` back into pinned host memory."""
+        if self.h_out is None:
+            self.h_out = [self.torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in ds.outputs]
         nbytes = 0
-        for h, d in zip(self.h_outs, self.d_outs):
-            h.copy_(d, non_blocking=True)
-            nbytes += d.numel() * d.element_size()
+        with self.torch.cuda.stream(stream):
+            for h, d in zip(self.h_out, ds.outputs):
+                h.copy_(d, non_blocking=True)
+                nbytes += d.numel() * d.element_size()
         return nbytes
+
+    def e2e(self, steps, warmup=2):
+        """Steady-state end-to-end throughput of the public API with host
+        buffers: every step copies its inputs in (H2D stream), runs the step
+        (compute stream) and reads its results back (D2H stream); two device
+        sets let step i's readback overlap step i+1's input copy and kernels.
+        Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
+        torch = self.torch
+        s_in = torch.cuda.Stream(self.dev)
+        s_run = torch.cuda.Stream(self.dev)
+        s_out = torch.cuda.Stream(self.dev)
+        self.sets = [DeviceSet(self, s_run), DeviceSet(self, s_run)]
+        Ev = torch.cuda.Event
+        # the copy engines alone, for reference: one step's inputs in, outputs
+        # out (best of three, after a warm-up copy)
+        self.copy_gbps = {}
+        for name, fn, st in (("h2d", self.h2d, s_in), ("d2h", self.d2h, s_out)):
+            fn(self.sets[0], st)
+            torch.cuda.synchronize(self.dev)
+            best = 0.0
+            for _ in range(3):
+                a, b = Ev(enable_timing=True), Ev(enable_timing=True)
+                a.record(st)
+                nb = fn(self.sets[0], st)
+                b.record(st)
+                torch.cuda.synchronize(self.dev)
+                best = max(best, nb / (a.elapsed_time(b) * 1e-3) / 1e9)
+            self.copy_gbps[name] = round(best, 1)
+        bi = bo = 0
+        total = warmup + steps
+        done_run = [None, None]      # compute of the set's previous step finished (inputs free)
+        done_out = [None, None]      # readback of the set's previous step finished (outputs free)
+        start = Ev(enable_timing=True)
+        end = Ev(enable_timing=True)
+        for i in range(total):
+            if i == warmup:
+                torch.cuda.synchronize(self.dev)
+                start.record(s_in)
+            ds = self.sets[i % 2]
+            if done_run[i % 2] is not None:
+                s_in.wait_event(done_run[i % 2])
+            bi = self.h2d(ds, s_in)
+            copied = Ev()
+            copied.record(s_in)
+            s_run.wait_event(copied)
+            if done_out[i % 2] is not None:
+                s_run.wait_event(done_out[i % 2])
+            ds.run()
+            ran = Ev()
+            ran.record(s_run)
+            done_run[i % 2] = ran
+            s_out.wait_event(ran)
+            bo = self.d2h(ds, s_out)
+            out = Ev()
+            out.record(s_out)
+            done_out[i % 2] = out
+        end.record(s_out)
+        torch.cuda.synchronize(self.dev)
+        # the sets were built for the pipeline streams; set 0 goes back to the main stream
+        self.sets = [DeviceSet(self, self.stream)]
+        self.h2d(self.sets[0], self.stream)
+        self.sets[0].run()
+        self.launches = self.sets[0].launches
+        torch.cuda.synchronize(self.dev)
+        return start.elapsed_time(end) / steps, bi, bo
 
 
 # --------------------------------------------------------- oracle runs ----
@@ -446,7 +554,7 @@ def fused_vs_naive(wl, torch, reps=20):
     ws = torch.empty(k * stride, dtype=torch.float32, device=wl.dev)
     ob, of = wl.red[0]
     s = vp(wl.stream.cuda_stream)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=wl.dev)
+    flush = L2Flush(torch, wl.dev)
 
     def fused():
         return L.fp8q_dequant_reduce(cp, sp, k, n, 0, vp(ob.data_ptr()), vp(of.data_ptr()), s)
@@ -460,7 +568,7 @@ def fused_vs_naive(wl, torch, reps=20):
             fn()
         tot = 0.0
         for _ in range(reps):
-            flush.fill_(3)
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(wl.stream)
             if fn() != 0:
@@ -476,6 +584,48 @@ def fused_vs_naive(wl, torch, reps=20):
     return out
 
 
+def ring_sweep(wl, torch, payloads=(64 << 20, 256 << 20), reps=10):
+    """One ring hop (e4m3, with the bf16 output of the last hop) at large
+    per-hop payloads, outside the step: the size range the >= 70%-of-peak
+    bar is stated for."""
+    import gen
+    L = wl.L
+    vp = ctypes.c_void_p
+    s = vp(wl.stream.cuda_stream)
+    flush = L2Flush(torch, wl.dev)
+    out = {}
+    for payload in payloads:
+        n = payload // 2
+        x0 = gen.ring_partial(0, n).to(wl.dev)
+        x1 = gen.ring_partial(1, n).to(wl.dev)
+        c0 = torch.empty(n, dtype=torch.uint8, device=wl.dev)
+        s0 = torch.empty(nscales(n), dtype=torch.float32, device=wl.dev)
+        c1 = torch.empty_like(c0)
+        s1 = torch.empty_like(s0)
+        ob = torch.empty(n, dtype=torch.bfloat16, device=wl.dev)
+        if L.fp8q_quantize_blockwise(vp(x0.data_ptr()), n, 0, vp(c0.data_ptr()), vp(s0.data_ptr()), s) != 0:
+            raise RuntimeError("ring sweep quantize failed")
+        args = (vp(c0.data_ptr()), vp(s0.data_ptr()), vp(x1.data_ptr()), ctypes.c_size_t(n), ctypes.c_int(0),
+                vp(c1.data_ptr()), vp(s1.data_ptr()), vp(ob.data_ptr()), s)
+        for _ in range(3):
+            L.fp8q_ring_hop(*args)
+        tot = 0.0
+        for _ in range(reps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(wl.stream)
+            if L.fp8q_ring_hop(*args) != 0:
+                raise RuntimeError("ring sweep hop failed")
+            b.record(wl.stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        us = 1e3 * tot / reps
+        nbytes = bytes_hop(n, True)
+        out[f"{payload >> 20}MiB"] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1)}
+        del x0, x1, c0, s0, c1, s1, ob
+    return out
+
+
 # ---------------------------------------------------------------- main ----
 def main():
     ap = argparse.ArgumentParser()
@@ -483,7 +633,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
                     help="launch one kernel of the step a few times on its bench inputs and exit (for ncu)")
@@ -513,12 +663,12 @@ def main():
             dist.barrier()
 
     wl = Workload(dev, rank, torch)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     warmup = max(args.warmup, 3)
     steps = max(args.steps, 1)
     nl = len(wl.launches)
     for _ in range(warmup):
-        flush.fill_(1)
+        flush()
         wl.run()
     torch.cuda.synchronize()
 
@@ -535,7 +685,7 @@ def main():
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        flush.fill_(i & 0xFF)                      # evict L2 between steps
+        flush()                                     # evict L2 between steps
         step_ev[i][0].record(wl.stream)
         wl.run(launch_ev[i])
         step_ev[i][1].record(wl.stream)
@@ -560,30 +710,16 @@ def main():
     value_gbs = bytes_all / (ms_step * 1e-3) / 1e9
 
     # ---------------- end to end: host buffers through the C ABI -----------
-    wl.alloc_host_outputs()
-    e2e_steps = max(1, min(args.e2e_steps, steps))
-    for _ in range(2):
-        wl.h2d()
-        wl.run()
-        wl.d2h()
-    torch.cuda.synchronize()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     barrier()
-    bi = bo = 0
-    for i in range(e2e_steps):
-        e2e_ev[i][0].record(wl.stream)
-        bi = wl.h2d()
-        wl.run()
-        bo = wl.d2h()
-        e2e_ev[i][1].record(wl.stream)
-    torch.cuda.synchronize()
+    e2e_local, bi, bo = wl.e2e(max(1, min(args.e2e_steps, steps)))
     barrier()
     clocks.stop()
-    e2e_ms, _, _ = combine_over_ranks(dist if world > 1 else None, dev,
-                                      sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps, 0.0, 0.0)
+    e2e_ms, _, _ = combine_over_ranks(dist if world > 1 else None, dev, e2e_local, 0.0, 0.0)
     e2e_gbs = bytes_all / (e2e_ms * 1e-3) / 1e9
+    e2e_steps = max(1, min(args.e2e_steps, steps))
 
     fvn = fused_vs_naive(wl, torch)
+    sweep = ring_sweep(wl, torch)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -608,7 +744,7 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "bucket_elements_per_shard": wl.n, "shards": wl.k,
                    "layer_weights": sum(b * m * k for _, b, m, k in wl.tensors), "launches_per_step": nl,
-                   "l2": "flushed between steps (256 MiB write outside the step events)",
+                   "l2": "flushed between steps (256 MiB write, then 256 MiB read, outside the step events)",
                    "io": "bf16 in; e4m3/e5m2 codes + fp32 scales, E8M0 swizzled scales, bf16/fp32 sums out"},
         "elements_per_s": round(elems_all / (ms_step * 1e-3), 1),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
@@ -617,9 +753,12 @@ def main():
                      "algorithmic_bytes_per_launch": dd["bytes"] // dd["launches"]},
         "kernels": kernels,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps},
+                "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
+                "copy_GBps_alone": getattr(wl, "copy_gbps", None),
+                "pipeline": "H2D, kernels and D2H on three streams, two device buffer sets"},
         "gpu_launches": nl * steps,
         "fused_vs_naive_reduce": fvn,
+        "ring_hop_sweep": {k: dict(v, frac_of_peak=round(v["GB/s"] / peak, 4)) for k, v in sweep.items()},
         "clocks": clock_info,
         "cpu_baseline": None,
     }

@@ -109,6 +109,53 @@ fp8q_status_t fp8q_ring_hop(const uint8_t* in_codes, const float* in_scales, con
                             size_t n, fp8q_format_t fmt, uint8_t* out_codes, float* out_scales,
                             void* out_bf16, fp8q_stream_t stream);
 
+/* One hop of a grouped call: the arguments of fp8q_ring_hop. */
+typedef struct {
+    const uint8_t* in_codes;   /* n codes (in)                                 */
+    const float* in_scales;    /* fp8q_num_scales(n) scales (in)               */
+    const void* local_bf16;    /* n bf16 (in)                                  */
+    size_t n;
+    uint8_t* out_codes;        /* n codes (out)                                */
+    float* out_scales;         /* fp8q_num_scales(n) scales (out)              */
+    void* out_bf16;            /* n bf16 (out), or NULL                        */
+} fp8q_hop_t;
+
+#define FP8Q_MAX_HOP_GROUP 16
+
+/* fp8q_ring_hop for up to FP8Q_MAX_HOP_GROUP independent hops in one launch
+ * (for instance the hops every rank of a ring makes in one step).  `hops` is
+ * a HOST array; every hop is checked as by fp8q_ring_hop, no output may
+ * overlap any input or output of the group except a hop's out_bf16 written
+ * in place over its own local_bf16, and count must be in
+ * [1, FP8Q_MAX_HOP_GROUP] (FP8Q_ERR_SIZE).  Results are those of one
+ * fp8q_ring_hop per hop. */
+fp8q_status_t fp8q_ring_hop_group(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, fp8q_stream_t stream);
+
+/* ---------------------------------------------------- ring AllReduce ----
+ * A ring AllReduce carried on the FP8 wire format, with all P ranks held on
+ * one GPU ([P1] ring-based collectives on the FP8 wire; [P2] a ring
+ * AllReduce moves 2 (P-1)/P of the bytes per GPU).  Chunk c of n elements is
+ * [c n/P, (c+1) n/P).
+ *   reduce-scatter: step 0, rank i quantizes its chunk i; steps 1..P-1,
+ *     rank i makes one fp8q_ring_hop on the message of rank i-1 (chunk
+ *     (i-s) mod P) with its own chunk, all P hops of a step in one launch;
+ *     rank i ends with chunk (i+1) mod P summed over all ranks, as codes;
+ *   all-gather: the reduced codes and scales travel unchanged, and every
+ *     rank dequantizes the whole vector into results[r] (all ranks equal).
+ * A sum, not a mean.
+ *   partials, results : HOST arrays of `ranks` device pointers to n bf16;
+ *                       results[r] may be partials[r] (in place)
+ *   ranks             : 2 .. FP8Q_MAX_HOP_GROUP (FP8Q_ERR_K otherwise)
+ *   n                 : a multiple of 512 * ranks (FP8Q_ERR_SIZE otherwise)
+ *   workspace         : fp8q_ring_allreduce_workspace_bytes(ranks, n) bytes of
+ *                       device memory, caller-owned (message and result codes)
+ *   wire_bytes        : if not NULL, the bytes one rank sends over the whole
+ *                       collective: 2 (P-1) (n/P) (1 + 4/128). */
+size_t fp8q_ring_allreduce_workspace_bytes(int ranks, size_t n);
+fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, void* const* results, int ranks, size_t n,
+                                      fp8q_format_t fmt, void* workspace, size_t workspace_bytes,
+                                      uint64_t* wire_bytes, fp8q_stream_t stream);
+
 /* ---------------------------------------------------------------- (d) ----
  * BF16 -> MXFP8 weight prequantization ([P3] Summary, self-review).
  * w is [batch, m, k] row-major ([out, in] weights, batch = experts); every
@@ -127,6 +174,48 @@ fp8q_status_t fp8q_ring_hop(const uint8_t* in_codes, const float* in_scales, con
 fp8q_status_t mxfp8_quantize_swizzled(const void* w_bf16, int64_t batch, int64_t m, int64_t k,
                                       uint8_t* codes, uint8_t* scales_swizzled, fp8q_stream_t stream);
 
+/* One weight tensor of a grouped MXFP8 call: the arguments of
+ * mxfp8_quantize_swizzled for that tensor. */
+typedef struct {
+    const void* w_bf16;        /* [batch, m, k] bf16, row-major (in)        */
+    int64_t batch, m, k;
+    uint8_t* codes;            /* batch * m * k E4M3 codes (out)            */
+    uint8_t* scales_swizzled;  /* mxfp8_swizzled_scale_bytes() bytes (out)  */
+} mxfp8_tensor_t;
+
+#define MXFP8_MAX_GROUP 16
+
+/* mxfp8_quantize_swizzled for up to MXFP8_MAX_GROUP tensors in one launch
+ * (for instance a decoder layer: the expert batches and the attention
+ * matrices), the way [P3] batches its MXFP8 MoE shuffle over all experts of
+ * a layer.  `tensors` is a HOST array of `count` descriptors; every tensor
+ * is checked as by mxfp8_quantize_swizzled (same status codes), no output
+ * may overlap any input or output of the group (FP8Q_ERR_ALIAS), and
+ * count must be in [1, MXFP8_MAX_GROUP] (FP8Q_ERR_SIZE).  Empty tensors are
+ * skipped.  Results are those of one mxfp8_quantize_swizzled per tensor. */
+fp8q_status_t mxfp8_quantize_swizzled_group(const mxfp8_tensor_t* tensors, int count, fp8q_stream_t stream);
+
+/* ------------------------------------------------------ MXFP8 receiver ----
+ * The receiving side of [P3]'s prequantized transfer.
+ *
+ * mxfp8_dequantize_swizzled: w = RNE_bf16(decode_e4m3(c) * 2^(e - 127)) for
+ *   codes [batch, m, k] and the swizzled E8M0 bytes of mxfp8_quantize_swizzled;
+ *   the product is exact, only results below the bf16 range round.
+ *   out_bf16: batch*m*k bf16 (out).  Same shape rules as the quantizer.
+ * mxfp8_unswizzle_scales: the E8M0 bytes in plain row-major order
+ *   [batch, m, k/32] (the layout whose trailing k/32 dimension [P3]'s inline
+ *   review insists on keeping, even when it is 1).
+ * fp8q_count_mismatches: adds to the device counter *count the number of
+ *   bytes where a and b differ (the bit-exact check [P3]'s reproductions
+ *   ran on the shuffled MXFP8 buffers); the caller zeroes *count.  count must
+ *   be 8-byte aligned device memory. */
+fp8q_status_t mxfp8_dequantize_swizzled(const uint8_t* codes, const uint8_t* scales_swizzled, int64_t batch,
+                                        int64_t m, int64_t k, void* out_bf16, fp8q_stream_t stream);
+fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, int64_t batch, int64_t m, int64_t k,
+                                     uint8_t* scales_rowmajor, fp8q_stream_t stream);
+fp8q_status_t fp8q_count_mismatches(const void* a, const void* b, size_t nbytes, unsigned long long* count,
+                                    fp8q_stream_t stream);
+
 /* ------------------------------------------------------------- helpers ---- */
 
 /* ceil(n / 128): the number of fp32 scales of an n-element blockwise array. */
@@ -141,6 +230,14 @@ const char* fp8q_status_string(fp8q_status_t status);
 
 /* cudaError_t of the most recent FP8Q_ERR_CUDA on the calling thread (0 if none). */
 int fp8q_last_cuda_error(void);
+
+/* Diagnostic, and the one call that synchronizes: waits for the current
+ * device, then returns in *flags the error bits the kernels raised since the
+ * last clear (0 = none; bit 0 = an input copy into shared memory did not land
+ * within 2 s, after which the kernel stopped and its outputs are invalid).
+ * Clears the bits when `clear` is non-zero. */
+#define FP8Q_DEVICE_ERR_COPY_TIMEOUT 1u
+fp8q_status_t fp8q_device_errors(unsigned int* flags, int clear);
 
 /* Plain satfinite round-to-nearest-even conversion of n binary32 values to
  * FP8 codes, with no scale (the element conversion step of (a) and (c),

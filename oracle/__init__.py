@@ -17,6 +17,8 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*``):
   dequant_reduce, ring_hop           pinned (exact rational sums within the
                                      fp32 recursive-summation bound)
   mxfp8 block codes and E8M0         pinned (hand examples, invariants)
+  mxfp8 dequantize / unswizzle       pinned (torch float8 decode times a power
+                                     of two; round trip; the hand swizzle table)
   scale swizzle                      formula pinned by a hand table and a
                                      bijection check; the layout itself is
                                      parity unpinned by the pages.
@@ -96,6 +98,10 @@ def lib() -> ctypes.CDLL:
         L.orc_swizzled_scale_bytes.restype = ctypes.c_uint64
         L.orc_mxfp8_quantize_swizzled.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _u8p]
         L.orc_mxfp8_quantize_swizzled.restype = ctypes.c_int
+        L.orc_mxfp8_unswizzle.argtypes = [_u8p, _i64, _i64, _i64, _u8p]
+        L.orc_mxfp8_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, _i64, _u16p]
+        L.orc_count_mismatches.argtypes = [_u8p, _u8p, _sz]
+        L.orc_count_mismatches.restype = ctypes.c_uint64
         _lib = L
     return _lib
 
@@ -245,3 +251,27 @@ def mxfp8_quantize_swizzled(w, batch: int, m: int, k: int):
     if rc != 0:
         raise ValueError("k must be a positive multiple of 32")
     return codes, scales[: swizzled_scale_bytes(batch, m, k)]
+
+
+def mxfp8_unswizzle(scales, batch: int, m: int, k: int) -> np.ndarray:
+    """Swizzled E8M0 bytes -> plain row-major [batch, m, k/32] uint8."""
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    out = np.empty(batch * m * (k // 32), np.uint8)
+    lib().orc_mxfp8_unswizzle(_p(scales, _u8p), batch, m, k, _p(out, _u8p))
+    return out
+
+
+def mxfp8_dequantize(codes, scales, batch: int, m: int, k: int) -> np.ndarray:
+    """E4M3 codes + swizzled E8M0 scales -> bf16 bit patterns [batch*m*k]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8).ravel()
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    out = np.empty(batch * m * k, np.uint16)
+    lib().orc_mxfp8_dequantize(_p(codes, _u8p), _p(scales, _u8p), batch, m, k, _p(out, _u16p))
+    return out
+
+
+def count_mismatches(a, b) -> int:
+    a = np.ascontiguousarray(a, dtype=np.uint8).ravel()
+    b = np.ascontiguousarray(b, dtype=np.uint8).ravel()
+    assert a.size == b.size
+    return int(lib().orc_count_mismatches(_p(a, _u8p), _p(b, _u8p), a.size))

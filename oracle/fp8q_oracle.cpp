@@ -350,4 +350,36 @@ int orc_mxfp8_quantize_swizzled(const uint16_t* w, int64_t batch, int64_t m, int
     return 0;
 }
 
+// ----------------------------------------- MXFP8 receiver (unswizzle etc.) --
+// The receiving side of [P3]'s prequantized transfer: the E8M0 scales back
+// in plain row-major order [batch, m, k/32], and the weights decoded,
+// w = RNE_bf16(decode_e4m3(c) * 2^(e - 127)) (the product is exact in
+// binary64; only the bf16 rounding can lose bits, below 2^-133).
+void orc_mxfp8_unswizzle(const uint8_t* scales, int64_t batch, int64_t m, int64_t k, uint8_t* out) {
+    int64_t kb = k / 32;
+    for (int64_t bt = 0; bt < batch; ++bt)
+        for (int64_t r = 0; r < m; ++r)
+            for (int64_t j = 0; j < kb; ++j) out[(bt * m + r) * kb + j] = scales[orc_swizzle_offset(bt, r, j, m, kb)];
+}
+
+void orc_mxfp8_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t batch, int64_t m, int64_t k,
+                          uint16_t* out_bf16) {
+    int64_t kb = k / 32;
+    for (int64_t bt = 0; bt < batch; ++bt)
+        for (int64_t r = 0; r < m; ++r)
+            for (int64_t i = 0; i < k; ++i) {
+                size_t off = (size_t)((bt * m + r) * k + i);
+                int e = scales[orc_swizzle_offset(bt, r, i / 32, m, kb)];
+                double v = decode_exact(kE4M3, codes[off]) * std::ldexp(1.0, e - 127);
+                out_bf16[off] = f32_to_bf16((float)v);     // exact in binary32, then RNE to bf16
+            }
+}
+
+// Number of differing bytes (the bit-exact verify of a shuffled buffer).
+uint64_t orc_count_mismatches(const uint8_t* a, const uint8_t* b, size_t n) {
+    uint64_t c = 0;
+    for (size_t i = 0; i < n; ++i) c += a[i] != b[i];
+    return c;
+}
+
 }  // extern "C"

@@ -40,3 +40,13 @@ def build_lib():
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     return mod.build()
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors(request):
+    """After every GPU test: no kernel reported a copy that failed to land."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import weight_transfer_gb300 as w
+    assert w.fp8q_device_errors(clear=True) == 0, "a kernel raised a device error flag"

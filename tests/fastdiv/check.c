@@ -4,8 +4,8 @@
  * For a block scale s and an element x the codec needs q = RN(x / s).
  * The kernel computes, with y = RN(1/s) once per block:
  *     q0 = RN(x * y)
- *     r  = RN(x - q0 * s)          (one fused multiply-add)
- *     q1 = RN(q0 + r * y)          (one fused multiply-add)
+ *     r  = RN(q0 * s - x)          (one fused multiply-add)
+ *     q1 = RN(q0 - r * y)          (one fused multiply-add)
  * which is Markstein's correction step (P. Markstein, "Computation of
  * elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
  * Dev. 34(1), 1990; also "IA-64 and Elementary Functions", 2000).
@@ -47,8 +47,8 @@ static void* run(void* arg) {
         for (uint32_t xm = 0; xm < 128; ++xm) {
             const float x = f_of(0x3F800000u | (xm << 16));  /* bf16 significand, x in [1, 2) */
             const float q0 = x * y;
-            const float r = fmaf(-q0, s, x);
-            const float q1 = fmaf(r, y, q0);
+            const float r = fmaf(q0, s, -x);
+            const float q1 = fmaf(-r, y, q0);
             const float ref = x / s;
             J->bad += u_of(q1) != u_of(ref);
         }
@@ -72,8 +72,8 @@ static int random_f32(uint64_t count, uint64_t seed) {
         const float y = 1.0f / s;
         float q = x * y;
         for (int c = 0; c < 2; ++c) {
-            const float e = fmaf(-q, s, x);
-            q = fmaf(e, y, q);
+            const float e = fmaf(q, s, -x);
+            q = fmaf(-e, y, q);
         }
         bad += u_of(q) != u_of(x / s);
     }

@@ -142,3 +142,47 @@ def test_binding_rejects_cpu_tensors():
     with pytest.raises(ValueError):
         w.fp8q_quantize_blockwise(torch.zeros(256, dtype=torch.bfloat16),
                                   codes=torch.zeros(1), scales=torch.zeros(1))
+
+
+def test_mxfp8_group_validation(L):
+    import weight_transfer_gb300 as w
+    T = w.mxfp8_tensor_t
+    f = L.mxfp8_quantize_swizzled_group
+    ok = T(A, 1, 128, 64, A + 64 * MB, A + 128 * MB)
+    arr = (T * 17)(*([ok] * 17))
+    assert f(arr, 0, None) == ERR_SIZE
+    assert f(arr, 17, None) == ERR_SIZE
+    assert f(None, 1, None) == ERR_NULL
+    bad_k = (T * 2)(ok, T(A + 200 * MB, 1, 128, 48, A + 264 * MB, A + 328 * MB))
+    assert f(bad_k, 2, None) == ERR_K
+    # tensor 1 writes its codes over tensor 0's input
+    alias = (T * 2)(ok, T(A + 200 * MB, 1, 128, 64, A + 1024, A + 328 * MB))
+    assert f(alias, 2, None) == ERR_ALIAS
+    empty = (T * 2)(T(None, 0, 128, 64, None, None), T(None, 1, 0, 64, None, None))
+    assert f(empty, 2, None) == OK
+
+
+def test_ring_group_and_allreduce_validation(L):
+    import weight_transfer_gb300 as w
+    H = w.fp8q_hop_t
+    g = L.fp8q_ring_hop_group
+    ok = H(A, A + MB, A + 2 * MB, 1024, A + 3 * MB, A + 4 * MB, None)
+    arr = (H * 17)(*([ok] * 17))
+    assert g(arr, 0, 0, None) == ERR_SIZE
+    assert g(arr, 17, 0, None) == ERR_SIZE
+    assert g(arr, 1, 9, None) == ERR_FORMAT
+    # two hops writing the same output codes
+    two = (H * 2)(ok, H(A + 10 * MB, A + 11 * MB, A + 12 * MB, 1024, A + 3 * MB, A + 14 * MB, None))
+    assert g(two, 2, 0, None) == ERR_ALIAS
+    empty = (H * 1)(H(None, None, None, 0, None, None, None))
+    assert g(empty, 1, 0, None) == OK
+    assert L.fp8q_ring_allreduce_workspace_bytes(8, 13_107_200) > 0
+    assert L.fp8q_ring_allreduce_workspace_bytes(8, 1000) == 0
+    assert L.fp8q_ring_allreduce_workspace_bytes(1, 1024) == 0
+    pp = (ctypes.c_void_p * 2)(A, A + 10 * MB)
+    rp = (ctypes.c_void_p * 2)(A + 20 * MB, A + 30 * MB)
+    r = L.fp8q_ring_allreduce_sim
+    assert r(pp, rp, 1, 1024, 0, A + 40 * MB, 1 << 20, None, None) == ERR_K
+    assert r(pp, rp, 2, 1000, 0, A + 40 * MB, 1 << 20, None, None) == ERR_SIZE
+    assert r(pp, rp, 2, 1024, 0, A + 40 * MB, 16, None, None) == ERR_SIZE       # workspace too small
+    assert r(pp, rp, 2, 0, 0, None, 0, None, None) == OK

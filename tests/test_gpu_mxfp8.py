@@ -99,3 +99,67 @@ def test_mxfp8_qwen3_layer_full_size(w, orc):
         assert_same(u8(c).ravel(), ec, f"{name} codes")
         del c, s, x
     pool.shutdown()
+
+
+def test_mxfp8_group_mixed_shapes_equals_per_tensor_oracle(w, orc):
+    shapes = [(1, 1, 32), (3, 129, 96), (1, 0, 64), (2, 256, 768), (1, 300, 2048), (5, 64, 160), (1, 127, 64)]
+    bits = [weight_bits(b, m, k, seed=70 + i) if b * m * k else np.zeros(0, np.uint16)
+            for i, (b, m, k) in enumerate(shapes)]
+    xs = [bf16_from_bits(x).view(b, m, k) for x, (b, m, k) in zip(bits, shapes)]
+    codes, scales = w.mxfp8_quantize_swizzled_group(xs)
+    torch.cuda.synchronize()
+    for x, c, s, (b, m, k) in zip(bits, codes, scales, shapes):
+        ec, es = orc.mxfp8_quantize_swizzled(x, b, m, k)
+        assert_same(u8(s), es, f"scales {b}x{m}x{k}")
+        assert_same(u8(c).ravel(), ec, f"codes {b}x{m}x{k}")
+
+
+def test_mxfp8_group_whole_qwen3_layer(w, orc):
+    # all 7 tensors of a Qwen3-30B-A3B-shaped layer (layer 1) in one launch,
+    # checked in full against the oracle run per tensor on expert slices
+    pool = cf.ThreadPoolExecutor(16)
+    xs = [gen.qwen3_tensor(1, t) for t in range(len(gen.QWEN3_TENSORS))]
+    codes, scales = w.mxfp8_quantize_swizzled_group([x.cuda() for x in xs])
+    torch.cuda.synchronize()
+    for t, (name, b, m, k) in enumerate(gen.QWEN3_TENSORS):
+        hb = bits16(xs[t]).reshape(b, m * k)
+        step = max(1, b // 16)
+        jobs = [(i, min(b, i + step)) for i in range(0, b, step)]
+        res = list(pool.map(lambda ij: orc.mxfp8_quantize_swizzled(hb[ij[0]:ij[1]].copy(), ij[1] - ij[0], m, k), jobs))
+        assert_same(u8(scales[t]), np.concatenate([r[1] for r in res]), f"{name} scales")
+        assert_same(u8(codes[t]).ravel(), np.concatenate([r[0] for r in res]), f"{name} codes")
+    pool.shutdown()
+
+
+# ----------------------------------------------------------- receiver side
+@pytest.mark.parametrize("b,m,k", [(1, 1, 32), (3, 129, 96), (2, 256, 768), (1, 300, 2048)])
+def test_mxfp8_dequantize_and_unswizzle(w, orc, b, m, k):
+    # inputs from the oracle's quantizer, plus random codes with random scale
+    # bytes (every e8m0 value, subnormal results included)
+    bits = weight_bits(b, m, k, seed=b + m + k)
+    codes, sc = orc.mxfp8_quantize_swizzled(bits, b, m, k)
+    rng = np.random.default_rng(b * m + k)
+    rcodes = rng.integers(0, 256, codes.size, dtype=np.uint8)
+    rcodes[(rcodes & 0x7F) == 0x7F] = 0x41
+    rsc = rng.integers(0, 255, sc.size, dtype=np.uint8)
+    for cc, ss in ((codes, sc), (rcodes, rsc)):
+        dc = torch.from_numpy(cc.reshape(b, m, k).copy()).cuda()
+        ds = torch.from_numpy(ss.copy()).cuda()
+        out = w.mxfp8_dequantize_swizzled(dc, ds)
+        plain = w.mxfp8_unswizzle_scales(ds, b, m, k)
+        torch.cuda.synchronize()
+        assert_same(bits16(out).ravel(), orc.mxfp8_dequantize(cc, ss, b, m, k), "dequantized weights")
+        assert_same(u8(plain).ravel(), orc.mxfp8_unswizzle(ss, b, m, k), "row-major scales")
+
+
+def test_count_mismatches(w, orc):
+    rng = np.random.default_rng(5)
+    for n in (1, 15, 16, 17, 4096 + 7, 3_000_001):
+        a = rng.integers(0, 256, n, dtype=np.uint8)
+        b = a.copy()
+        flip = rng.choice(n, size=min(n, 1 + n // 1000), replace=False)
+        b[flip] ^= rng.integers(1, 256, flip.size, dtype=np.uint8)
+        got = w.fp8q_count_mismatches(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+        same = w.fp8q_count_mismatches(torch.from_numpy(a).cuda(), torch.from_numpy(a).cuda())
+        assert int(got.item()) == orc.count_mismatches(a, b) == flip.size
+        assert int(same.item()) == 0

@@ -470,3 +470,51 @@ def test_mxfp8_codes_to_scales_ratio(orc):
 def test_mxfp8_rejects_k_not_multiple_of_32(orc):
     with pytest.raises(ValueError):
         orc.mxfp8_quantize_swizzled(np.zeros(48, np.uint16), 1, 1, 48)
+
+
+# ----------------------------------------------------- MXFP8 receiver -----
+def test_mxfp8_dequantize_is_exact_power_of_two_scaling(orc):
+    # every code times 2^(e-127), computed in float64 from torch's e4m3
+    # decode and cast to bf16 by torch, for many scale bytes
+    rng = np.random.default_rng(81)
+    b, m, k = 2, 130, 96
+    codes = rng.integers(0, 256, b * m * k, dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3C
+    kb = k // 32
+    plain = rng.integers(0, 255, b * m * kb, dtype=np.uint8)
+    sc = np.zeros(orc.swizzled_scale_bytes(b, m, k), np.uint8)
+    for bt in range(b):
+        for r in range(m):
+            for j in range(kb):
+                sc[orc.swizzle_offset(bt, r, j, m, kb)] = plain[(bt * m + r) * kb + j]
+    got = orc.mxfp8_dequantize(codes, sc, b, m, k)
+    e = np.repeat(plain.astype(np.int64), 32)
+    val = torch_fp8_decode(0, codes).astype(np.float64) * np.exp2(e - 127.0)
+    want = torch.from_numpy(val.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+    assert np.array_equal(orc.mxfp8_unswizzle(sc, b, m, k), plain)
+
+
+def test_mxfp8_round_trip_within_half_ulp(orc):
+    rng = np.random.default_rng(82)
+    m, k = 64, 256
+    w = (rng.standard_normal(m * k) * 0.02).astype(np.float32)
+    wb = bf16_bits(w)
+    codes, sc = orc.mxfp8_quantize_swizzled(wb, 1, m, k)
+    back = bf16_val(orc.mxfp8_dequantize(codes, sc, 1, m, k)).astype(np.float64)
+    wv = bf16_val(wb).astype(np.float64)
+    e = orc.mxfp8_unswizzle(sc, 1, m, k).astype(np.int64)
+    unit = np.exp2(np.repeat(e, 32) - 127.0)            # the block's 2^(e-127)
+    scaled = np.abs(wv) / unit                           # in [0, 512)
+    # |error| <= half an e4m3 ulp of the scaled value (<= 16 below 512), or
+    # the saturation above 448, times the scale
+    bound = np.maximum(16.0, scaled - 448.0) * unit
+    assert (np.abs(back - wv) <= bound + 2.0 ** -133).all()
+    assert (scaled < 512).all()
+
+
+def test_count_mismatches(orc):
+    a = np.arange(1000, dtype=np.uint32).astype(np.uint8)
+    b = a.copy()
+    b[[3, 500, 999]] ^= 1
+    assert orc.count_mismatches(a, a) == 0 and orc.count_mismatches(a, b) == 3

@@ -45,16 +45,44 @@ _sz = ctypes.c_size_t
 _i64 = ctypes.c_int64
 _int = ctypes.c_int
 
+
+class fp8q_hop_t(ctypes.Structure):
+    """One hop of fp8q_ring_hop_group (same layout as the C struct)."""
+    _fields_ = [("in_codes", ctypes.c_void_p), ("in_scales", ctypes.c_void_p), ("local_bf16", ctypes.c_void_p),
+                ("n", ctypes.c_size_t), ("out_codes", ctypes.c_void_p), ("out_scales", ctypes.c_void_p),
+                ("out_bf16", ctypes.c_void_p)]
+
+
+FP8Q_MAX_HOP_GROUP = 16
+
+
+class mxfp8_tensor_t(ctypes.Structure):
+    """One tensor of mxfp8_quantize_swizzled_group (same layout as the C struct)."""
+    _fields_ = [("w_bf16", _vp), ("batch", _i64), ("m", _i64), ("k", _i64), ("codes", _vp),
+                ("scales_swizzled", _vp)]
+
+
+MXFP8_MAX_GROUP = 16
+
 # name -> (argtypes, restype)
 _SIGNATURES = {
     "fp8q_quantize_blockwise": ([_vp, _sz, _int, _vp, _vp, _vp], _int),
     "fp8q_dequant_reduce": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, _vp], _int),
     "fp8q_ring_hop": ([_vp, _vp, _vp, _sz, _int, _vp, _vp, _vp, _vp], _int),
     "mxfp8_quantize_swizzled": ([_vp, _i64, _i64, _i64, _vp, _vp, _vp], _int),
+    "mxfp8_quantize_swizzled_group": ([ctypes.POINTER(mxfp8_tensor_t), _int, _vp], _int),
+    "mxfp8_dequantize_swizzled": ([_vp, _vp, _i64, _i64, _i64, _vp, _vp], _int),
+    "mxfp8_unswizzle_scales": ([_vp, _i64, _i64, _i64, _vp, _vp], _int),
+    "fp8q_count_mismatches": ([_vp, _vp, _sz, _vp, _vp], _int),
+    "fp8q_ring_hop_group": ([ctypes.POINTER(fp8q_hop_t), _int, _int, _vp], _int),
+    "fp8q_ring_allreduce_workspace_bytes": ([_int, _sz], _sz),
+    "fp8q_ring_allreduce_sim": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _sz,
+                                 ctypes.POINTER(ctypes.c_uint64), _vp], _int),
     "fp8q_num_scales": ([_sz], _sz),
     "mxfp8_swizzled_scale_bytes": ([_i64, _i64, _i64], _sz),
     "fp8q_status_string": ([_int], ctypes.c_char_p),
     "fp8q_last_cuda_error": ([], _int),
+    "fp8q_device_errors": ([ctypes.POINTER(ctypes.c_uint), _int], _int),
     "fp8q_encode_f32": ([_vp, _sz, _int, _vp, _vp], _int),
     "fp8q_dequantize": ([_vp, _vp, _sz, _int, _vp, _vp, _vp], _int),
     "fp8q_unfused_stride": ([_sz], _sz),
@@ -118,6 +146,13 @@ def _stream(stream) -> int:
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
+
+
+def fp8q_device_errors(clear: bool = True) -> int:
+    """Synchronizes the device and returns the kernels' error bits (0 = none)."""
+    v = ctypes.c_uint(0)
+    _check("fp8q_device_errors", lib().fp8q_device_errors(ctypes.byref(v), int(clear)))
+    return int(v.value)
 
 
 def fp8q_num_scales(n: int) -> int:
@@ -213,6 +248,137 @@ def mxfp8_quantize_swizzled(w: torch.Tensor, codes: Optional[torch.Tensor] = Non
                                        _dev(scales_swizzled, "scales_swizzled", torch.uint8, sb), _stream(stream))
     _check("mxfp8_quantize_swizzled", st)
     return codes, scales_swizzled[:sb]
+
+
+def fp8q_ring_hop_group(hops: Sequence[dict], fmt="e4m3", stream=None):
+    """Several independent hops in one launch; each dict has the tensors
+    in_codes, in_scales, local and optionally out_codes, out_scales,
+    out_bf16 (allocated when missing; out_bf16 only if want_bf16).  Returns
+    the list of (out_codes, out_scales, out_bf16 or None)."""
+    count = len(hops)
+    arr = (fp8q_hop_t * max(count, 1))()
+    outs = []
+    for i, hp in enumerate(hops):
+        loc = hp["local"]
+        n = loc.numel()
+        nb = fp8q_num_scales(n)
+        oc = hp.get("out_codes") if hp.get("out_codes") is not None else torch.empty(n, dtype=torch.uint8,
+                                                                                      device=loc.device)
+        os_ = hp.get("out_scales") if hp.get("out_scales") is not None else torch.empty(max(nb, 1),
+                                                                                        dtype=torch.float32,
+                                                                                        device=loc.device)
+        ob = hp.get("out_bf16")
+        if ob is None and hp.get("want_bf16"):
+            ob = torch.empty(n, dtype=torch.bfloat16, device=loc.device)
+        arr[i] = fp8q_hop_t(_dev(hp["in_codes"], f"hops[{i}].in_codes", torch.uint8, n),
+                            _dev(hp["in_scales"], f"hops[{i}].in_scales", torch.float32, nb),
+                            _dev(loc, f"hops[{i}].local", torch.bfloat16), n,
+                            _dev(oc, f"hops[{i}].out_codes", torch.uint8, n),
+                            _dev(os_, f"hops[{i}].out_scales", torch.float32, nb),
+                            _dev(ob, f"hops[{i}].out_bf16", torch.bfloat16, n))
+        outs.append((oc, os_, ob))
+    _check("fp8q_ring_hop_group", lib().fp8q_ring_hop_group(arr, count, _fmt(fmt), _stream(stream)))
+    return outs
+
+
+def fp8q_ring_allreduce_sim(partials: Sequence[torch.Tensor], fmt="e4m3", results: Optional[Sequence[torch.Tensor]] = None,
+                            workspace: Optional[torch.Tensor] = None, stream=None):
+    """Ring AllReduce of P ranks' bf16 vectors held on one GPU, over the FP8
+    wire format -> (list of P result tensors, wire bytes sent per rank)."""
+    P = len(partials)
+    n = partials[0].numel()
+    dev = partials[0].device
+    if results is None:
+        results = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    wb = int(lib().fp8q_ring_allreduce_workspace_bytes(P, n))
+    if workspace is None:
+        workspace = torch.empty(max(wb, 16), dtype=torch.uint8, device=dev)
+    pp = (_vp * P)(*[_dev(t, f"partials[{i}]", torch.bfloat16, n) for i, t in enumerate(partials)])
+    rp = (_vp * P)(*[_dev(t, f"results[{i}]", torch.bfloat16, n) for i, t in enumerate(results)])
+    wire = ctypes.c_uint64(0)
+    st = lib().fp8q_ring_allreduce_sim(pp, rp, P, n, _fmt(fmt), _dev(workspace, "workspace", torch.uint8),
+                                       workspace.numel(), ctypes.byref(wire), _stream(stream))
+    _check("fp8q_ring_allreduce_sim", st)
+    return list(results), int(wire.value)
+
+
+def mxfp8_quantize_swizzled_group(weights: Sequence[torch.Tensor], codes: Optional[Sequence[torch.Tensor]] = None,
+                                  scales: Optional[Sequence[torch.Tensor]] = None, stream=None):
+    """Several bf16 weights ([m, k] or [batch, m, k]) in one launch ->
+    (list of codes, list of swizzled scale buffers), as one
+    mxfp8_quantize_swizzled per weight would give."""
+    n = len(weights)
+    if n > MXFP8_MAX_GROUP:
+        raise ValueError(f"at most {MXFP8_MAX_GROUP} tensors per group")
+    arr = (mxfp8_tensor_t * max(n, 1))()
+    outc, outs = [], []
+    for i, w in enumerate(weights):
+        if w.dim() == 2:
+            b, (m, k) = 1, w.shape
+        elif w.dim() == 3:
+            b, m, k = w.shape
+        else:
+            raise ValueError("each weight must be 2D or 3D")
+        sb = mxfp8_swizzled_scale_bytes(b, m, k)
+        c = codes[i] if codes is not None else torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+        sc = scales[i] if scales is not None else torch.empty(max(sb, 16), dtype=torch.uint8, device=w.device)
+        arr[i] = mxfp8_tensor_t(_dev(w, f"weights[{i}]", torch.bfloat16), b, m, k,
+                                _dev(c, f"codes[{i}]", torch.uint8, b * m * k),
+                                _dev(sc, f"scales[{i}]", torch.uint8, sb))
+        outc.append(c)
+        outs.append(sc[:sb])
+    st = lib().mxfp8_quantize_swizzled_group(arr, n, _stream(stream))
+    _check("mxfp8_quantize_swizzled_group", st)
+    return outc, outs
+
+
+def _mx_shape(codes: torch.Tensor):
+    if codes.dim() == 2:
+        return 1, codes.shape[0], codes.shape[1]
+    if codes.dim() == 3:
+        return tuple(codes.shape)
+    raise ValueError("codes must be 2D [m, k] or 3D [batch, m, k]")
+
+
+def mxfp8_dequantize_swizzled(codes: torch.Tensor, scales_swizzled: torch.Tensor,
+                              out: Optional[torch.Tensor] = None, stream=None):
+    """E4M3 codes [m, k] / [batch, m, k] + swizzled E8M0 bytes -> bf16 weights."""
+    b, m, k = _mx_shape(codes)
+    if out is None:
+        out = torch.empty(codes.shape, dtype=torch.bfloat16, device=codes.device)
+    st = lib().mxfp8_dequantize_swizzled(_dev(codes, "codes", torch.uint8),
+                                         _dev(scales_swizzled, "scales_swizzled", torch.uint8,
+                                              mxfp8_swizzled_scale_bytes(b, m, k)),
+                                         b, m, k, _dev(out, "out", torch.bfloat16, b * m * k), _stream(stream))
+    _check("mxfp8_dequantize_swizzled", st)
+    return out
+
+
+def mxfp8_unswizzle_scales(scales_swizzled: torch.Tensor, batch: int, m: int, k: int,
+                           out: Optional[torch.Tensor] = None, stream=None):
+    """Swizzled E8M0 bytes -> row-major uint8 [batch, m, k // 32]."""
+    if out is None:
+        out = torch.empty((batch, m, k // 32), dtype=torch.uint8, device=scales_swizzled.device)
+    st = lib().mxfp8_unswizzle_scales(_dev(scales_swizzled, "scales_swizzled", torch.uint8,
+                                           mxfp8_swizzled_scale_bytes(batch, m, k)),
+                                      batch, m, k, _dev(out, "out", torch.uint8, batch * m * (k // 32)),
+                                      _stream(stream))
+    _check("mxfp8_unswizzle_scales", st)
+    return out
+
+
+def fp8q_count_mismatches(a: torch.Tensor, b: torch.Tensor, count: Optional[torch.Tensor] = None, stream=None):
+    """Number of differing bytes of two equally sized CUDA tensors (an int64
+    device tensor; pass `count` to accumulate into an existing one)."""
+    nbytes = a.numel() * a.element_size()
+    if b.numel() * b.element_size() != nbytes:
+        raise ValueError("a and b must have the same byte size")
+    if count is None:
+        count = torch.zeros(1, dtype=torch.int64, device=a.device)
+    st = lib().fp8q_count_mismatches(_dev(a, "a"), _dev(b, "b"), nbytes, _dev(count, "count", torch.int64, 1),
+                                     _stream(stream))
+    _check("fp8q_count_mismatches", st)
+    return count
 
 
 def fp8q_encode_f32(x: torch.Tensor, fmt="e4m3", codes: Optional[torch.Tensor] = None, stream=None):

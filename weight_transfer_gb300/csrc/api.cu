@@ -42,3 +42,12 @@ extern "C" const char* fp8q_status_string(fp8q_status_t status) {
     }
     return "unknown status";
 }
+
+extern "C" fp8q_status_t fp8q_device_errors(unsigned int* flags, int clear) {
+    if (!flags) return FP8Q_ERR_NULL;
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fp8q::cuda_status(e);
+    *flags = fp8q::unit_errors_quantize(clear != 0) | fp8q::unit_errors_reduce(clear != 0) |
+             fp8q::unit_errors_ring_hop(clear != 0) | fp8q::unit_errors_mxfp8(clear != 0);
+    return FP8Q_OK;
+}

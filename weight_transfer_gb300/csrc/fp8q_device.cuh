@@ -18,9 +18,17 @@ constexpr int kE5M2 = 1;
 
 // Largest finite magnitude of each OFP8 format (E4M3: 1.75 * 2^8,
 // E5M2: 1.75 * 2^15); the blockwise scale is amax divided by it.
+// `inverse` is RN(1 / value): 1.75 has the binary32 reciprocal
+// 0x1.24924ap-1 (1/1.75 = 0.571428..., rounded to nearest).
 template <int FMT> struct FmtMax;
-template <> struct FmtMax<kE4M3> { static constexpr float value = 448.0f; };
-template <> struct FmtMax<kE5M2> { static constexpr float value = 57344.0f; };
+template <> struct FmtMax<kE4M3> {
+    static constexpr float value = 448.0f;
+    static constexpr float inverse = 0x1.24924ap-9f;
+};
+template <> struct FmtMax<kE5M2> {
+    static constexpr float value = 57344.0f;
+    static constexpr float inverse = 0x1.24924ap-16f;
+};
 
 // ---------------------------------------------------------------- bf16 ----
 // A bf16 is the upper half of a binary32, so widening is a shift.
@@ -61,7 +69,7 @@ template <> __device__ __forceinline__ uint32_t cvt_fp8x2<kE5M2>(float lo, float
 // Four binary32 -> four codes in one 32-bit word (byte i = element i).
 template <int FMT>
 __device__ __forceinline__ uint32_t cvt_fp8x4(float a, float b, float c, float d) {
-    return cvt_fp8x2<FMT>(a, b) | (cvt_fp8x2<FMT>(c, d) << 16);
+    return __byte_perm(cvt_fp8x2<FMT>(a, b), cvt_fp8x2<FMT>(c, d), 0x5410u);
 }
 
 // Two codes (bytes 0 and 1 of `two`) -> two binary32.  Both formats embed
@@ -164,65 +172,172 @@ __device__ __forceinline__ void st_f32_tail(float* p, const float* f, int count,
         if (i < avail) p[i] = f[i];
 }
 
+// ------------------------------------------- bulk copies (TMA) to smem ----
+// The kernels stage their input tiles in shared memory with cp.async.bulk
+// (1D) or cp.async.bulk.tensor (2D tensor map).  Completion is tracked by
+// one mbarrier per stage ("transaction bytes"): the issuing thread arms the
+// barrier with the byte count, the copy engine counts the bytes down, and
+// the readers wait on the barrier's phase parity.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes freshly initialised barriers visible to the copy engine.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this CTA's earlier shared-memory accesses before later bulk copies
+// into the same bytes (generic proxy -> async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wall-clock bound of every wait on a copy: a copy that has not landed after
+// this long will never land, and the kernel reports it instead of hanging.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Waits until phase `parity` of the barrier has completed; false if that did
+// not happen within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 256; ++i)
+            if (mbar_test(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// 1D bulk copy global -> shared; both addresses 16-byte aligned, bytes a
+// multiple of 16.  Completes `bytes` transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(smem_dst)),
+                 "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// 2D tiled bulk copy of the box at (x, y) of a tensor map; x * element size
+// must be a multiple of 16 bytes, out-of-range elements read as zero.
+__device__ __forceinline__ void tma_2d_g2s(void* smem_dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Device-side error bits (see fp8q_device_errors).  Each translation unit
+// has its own word; the host ORs them together.
+constexpr unsigned kErrCopyTimeout = 1u;
+
+static __device__ unsigned int g_unit_errors;
+
+__device__ __forceinline__ void raise_error(unsigned bits) { atomicOr(&g_unit_errors, bits); }
+
+// Host side: this unit's error bits (the caller has synchronized the device).
+static inline unsigned read_unit_errors(bool clear) {
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_unit_errors, sizeof v) != cudaSuccess) return ~0u;
+    if (clear && v) {
+        const unsigned z = 0;
+        cudaMemcpyToSymbol(g_unit_errors, &z, sizeof z);
+    }
+    return v;
+}
+
 // --------------------------------------------------------------- scale ----
-// The block scale s = RN(amax / Fmax): a true IEEE binary32 division (the
-// compiler's correctly rounded div.rn.f32), once per block.
+// RN(x / d) by Markstein's correction step from y = RN(1/d):
+//     q0 = RN(x*y);  r = RN(q0*d - x) (fma);  q = RN(q0 - r*y) (fma)
+// (P. Markstein, IBM J. Res. Dev. 34(1), 1990; "IA-64 and Elementary
+// Functions", 2000).  The residual is formed negated, q0*d - x instead of
+// x - q0*d: both roundings are sign-symmetric so the result is the same for
+// every x != 0, and x = -0 then yields -0 (the plain form gives +0).
+//
+//  * One step is exact for bf16 dividends: it equals RN(x/d) for all 2^30
+//    pairs of a bf16 significand and a binary32 significand at unit scale
+//    (exhaustive check in tests/fastdiv/check.c).
+//  * Two steps are exact for binary32 dividends: one step leaves q within
+//    half an ulp plus a 2^-46-relative term of x/d, i.e. faithful, and
+//    Markstein's theorem (y = RN(1/d), q faithful => the next step gives
+//    RN(x/d)) covers the second.
+//
+// Every operation commutes with power-of-two scaling of x and d while all
+// intermediates stay normal binary32, which extends the unit-scale result to
+// all exponents for which x, d, y, q0 and a non-zero r are normal.  r is a
+// non-zero multiple of 2^(e_x - 47) (x has a 24-bit significand, q0*d a
+// 48-bit one), so |x| >= 2^-78 keeps it normal.
+template <int STEPS>
+__device__ __forceinline__ float markstein_div(float x, float d, float y) {
+    float q = __fmul_rn(x, y);
+#pragma unroll
+    for (int c = 0; c < STEPS; ++c) {
+        const float r = __fmaf_rn(q, d, -x);
+        q = __fmaf_rn(-r, y, q);
+    }
+    return q;
+}
+
+// The block scale s = RN(amax / Fmax), Fmax = 1.75 * 2^8 (e4m3) or
+// 1.75 * 2^15 (e5m2).  amax is a bf16 value, so one Markstein step from the
+// constant RN(1 / Fmax) is exact as long as amax / Fmax is a normal binary32
+// and amax >= 2^-78 (see markstein_div); smaller amax takes the IEEE division.
 template <int FMT>
 __device__ __forceinline__ float block_scale(float amax) {
-    return __fdiv_rn(amax, FmtMax<FMT>::value);
+    constexpr float F = FmtMax<FMT>::value;
+    return amax >= 0x1p-78f ? markstein_div<1>(amax, F, FmtMax<FMT>::inverse) : __fdiv_rn(amax, F);
 }
 
-// q = x / s for a block scale s; s == 0 only for an all-zero block, whose
-// elements are signed zeros and are passed through unchanged.
-__device__ __forceinline__ float scaled_quotient(float x, float s) {
-    return s == 0.0f ? x : __fdiv_rn(x, s);
-}
-
-__device__ __forceinline__ float with_sign_of(float mag, float sgn) {
-    return __uint_as_float((__float_as_uint(mag) & 0x7FFFFFFFu) | (__float_as_uint(sgn) & 0x80000000u));
-}
-
-// RN(x_i / s) for all elements of one block, without a per-element division.
+// RN(x_i / s) for all elements of one block, without a per-element division:
+// y = RN(1/s) once (rcp.rn, correctly rounded), then markstein_div with
+// STEPS = 1 for bf16 dividends and STEPS = 2 for binary32 dividends.
 //
-// With y = RN(1/s) computed once (rcp.rn, correctly rounded), each quotient
-// is q0 = RN(x*y) followed by CORRECTIONS Markstein steps
-//     r = RN(x - q*s)  (fma),   q = RN(q + r*y)  (fma)
-// (P. Markstein, IBM J. Res. Dev. 34(1), 1990; "IA-64 and Elementary
-// Functions", 2000).  The sign is taken from x so that x = -0 stays -0.
-//
-//  * CORRECTIONS = 1 is used for bf16 dividends.  It equals RN(x/s) for all
-//    2^30 pairs of a bf16 significand and a binary32 significand at unit
-//    scale (exhaustive check in tests/fastdiv/check.c).
-//  * CORRECTIONS = 2 is used for binary32 dividends.  One step leaves q
-//    within half an ulp plus a 2^-46-relative term of x/s, i.e. faithful;
-//    Markstein's theorem (y = RN(1/s), q faithful => RN(q + r*y) = RN(x/s))
-//    makes the second step exact.
-//
-// Every operation commutes with power-of-two scaling of x and s while all
-// intermediates are normal binary32.  That holds for every element whose
-// code can be non-zero (|x/s| >= 2^-20) as soon as s >= 2^-58: then
-// |x| >= 2^-78 and the residual r, a non-zero multiple of 2^(e_x - 47), is
-// at least 2^-125.  Elements with |x/s| < 2^-20 round to a signed-zero code
-// either way (the result stays far below the smallest FP8 subnormal, 2^-16).
-// Blocks with s < 2^-58 (amax < 448 * 2^-58 for e4m3) take the IEEE
-// division instead.
-template <int CORRECTIONS, int N>
+// For every element whose code can be non-zero (|x/s| >= 2^-20) the
+// conditions of markstein_div hold as soon as s >= 2^-58 (then |x| >= 2^-78).
+// Elements with |x/s| < 2^-20 round to a signed-zero code either way (the
+// result stays far below the smallest FP8 subnormal, 2^-16, and keeps the
+// sign of x).  Blocks with s < 2^-58 (amax < 448 * 2^-58 for e4m3) use the
+// IEEE division; s == 0 only for an all-zero block, whose signed zeros pass
+// through unchanged.
+template <int STEPS, int N>
 __device__ __forceinline__ void block_quotients(const float* x, float s, float* q) {
     if (s >= 0x1p-58f) {
         const float y = __frcp_rn(s);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            float t = __fmul_rn(x[i], y);
-#pragma unroll
-            for (int c = 0; c < CORRECTIONS; ++c) {
-                const float r = __fmaf_rn(-t, s, x[i]);
-                t = __fmaf_rn(r, y, t);
-            }
-            q[i] = with_sign_of(t, x[i]);
-        }
+        for (int i = 0; i < N; ++i) q[i] = markstein_div<STEPS>(x[i], s, y);
     } else {
 #pragma unroll
-        for (int i = 0; i < N; ++i) q[i] = scaled_quotient(x[i], s);
+        for (int i = 0; i < N; ++i) q[i] = s == 0.0f ? x[i] : __fdiv_rn(x[i], s);
     }
 }
 

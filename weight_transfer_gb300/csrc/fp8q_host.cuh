@@ -27,6 +27,13 @@ fp8q_status_t cuda_status(cudaError_t e);
 // Status of the launch just made on this thread.
 inline fp8q_status_t launch_status() { return cuda_status(cudaGetLastError()); }
 
+// Error bits raised by the kernels of each translation unit since the last
+// clear (read after the caller has synchronized the device).
+unsigned unit_errors_quantize(bool clear);
+unsigned unit_errors_reduce(bool clear);
+unsigned unit_errors_ring_hop(bool clear);
+unsigned unit_errors_mxfp8(bool clear);
+
 // SM count of the current device (cached per device).
 int sm_count();
 

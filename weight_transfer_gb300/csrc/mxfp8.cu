@@ -7,81 +7,184 @@
 // and inline review (a K/32 scale dimension of 1 is real).  Block rule from
 // the OCP MX v1.0 specification: e = floor(log2 amax) - 8 + 127 for E4M3.
 //
-// Work split: a CTA owns one 128-row x 128-column tile of one matrix, which
-// is exactly one 512-byte tile of the swizzled scale buffer (128 rows x 4
-// scale columns).  Each warp covers 16 rows, two rows per 16-byte load
-// instruction (16 lanes x 8 bf16 = 128 columns); 4 lanes share a 32-element
-// block and reduce its amax with two xor-shuffles.  The 512 scale bytes are
-// placed at their swizzled positions in shared memory and leave the CTA as
-// one contiguous 512-byte store; codes are written row-major.
+// Work split: a persistent CTA of 512 threads walks 128-row x 128-column
+// tiles of the [batch * m, k] row-major view of the weights; one tile is
+// exactly one 512-byte tile of the swizzled scale buffer (128 rows x 4 scale
+// columns).  Thread 0 keeps up to kMxStages tiles in flight, each a single
+// 2D tensor-map copy (cp.async.bulk.tensor, a 128 x 128 bf16 box = 32 KB)
+// into a shared-memory stage armed on its mbarrier; rows past the end of a
+// matrix belong to the next matrix or read as zeros and are ignored.  Each
+// warp then covers 8 rows, two rows per 16-byte shared-memory read (16
+// lanes x 8 bf16 = 128 columns, no bank conflicts); 4 lanes share a
+// 32-element block and reduce its amax with two xor-shuffles.  The 512 scale
+// bytes are placed at their swizzled positions in shared memory and leave
+// the CTA as one contiguous 512-byte store; codes are written row-major.
 //
 // The exponent needs no floating-point log: for a finite amax >= 0 with
 // biased binary32 exponent E, floor(log2 amax) - 8 + 127 = E - 8 when amax
 // is normal, and every subnormal or zero amax clamps to 0 -- so
 // e = max(E - 8, 0).  The scaling by 2^(127 - e) is exact (a power of two in
 // the normal range, 2^-119 .. 2^127).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
 namespace fp8q {
 
-constexpr int kMxThreads = 256;
-constexpr int kMxRowsPerWarp = 16;
+constexpr int kMxThreads = 512;
+constexpr int kMxRowsPerWarp = 128 / (kMxThreads / 32);
+constexpr int kMxStages = 3;
+constexpr int kMxStageBytes = 128 * 128 * 2;
+// stages (1024-byte aligned for the tensor copies), two 512-byte scale
+// tiles, the barriers, and slack to align the dynamic shared memory base
+constexpr size_t kMxSmem = (size_t)kMxStages * kMxStageBytes + 2 * 512 + 8 * kMxStages + 1024;
+
+// Up to kMxMaxGroup weight tensors quantized by one launch (a whole layer:
+// the expert batches and the attention matrices).  Tensor g owns the global
+// tiles [tile_start[g], tile_start[g + 1]).
+constexpr int kMxMaxGroup = MXFP8_MAX_GROUP;
+
+struct MxGroup {
+    CUtensorMap tmap[kMxMaxGroup];          // [batch * m, k] 16-bit view, 128 x 128 boxes
+    int64_t m[kMxMaxGroup];
+    int64_t k[kMxMaxGroup];
+    int64_t col_tiles[kMxMaxGroup];
+    int64_t tiles_per_mat[kMxMaxGroup];
+    int64_t tile_start[kMxMaxGroup + 1];
+    uint8_t* codes[kMxMaxGroup];
+    uint8_t* scales[kMxMaxGroup];
+    int count;
+};
+
+// Which tensor of the group global tile t belongs to (CTA-uniform).
+__device__ __forceinline__ int group_of(const MxGroup& g, int64_t t) {
+    int gi = 0;
+    while (gi + 1 < g.count && t >= g.tile_start[gi + 1]) ++gi;
+    return gi;
+}
 
 __global__ void __launch_bounds__(kMxThreads)
-mxfp8_quantize_kernel(const uint16_t* __restrict__ w, int64_t m, int64_t k, int64_t row_tiles,
-                      int64_t col_tiles, int64_t total_tiles, uint8_t* __restrict__ codes,
-                      uint8_t* __restrict__ scales) {
-    __shared__ __align__(16) uint8_t sbuf[2][512];
-    const unsigned lane = threadIdx.x & 31u;
-    const unsigned warp = threadIdx.x >> 5;
+mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t* sbuf = smem + kMxStages * kMxStageBytes;                 // [2][512]
+    uint64_t* full = reinterpret_cast<uint64_t*>(sbuf + 2 * 512);
+    const unsigned tid = threadIdx.x;
+    const unsigned lane = tid & 31u;
+    const unsigned warp = tid >> 5;
     const unsigned c = lane & 15u;                 // 8-column chunk inside the tile
     const unsigned jl = c >> 2;                    // scale column inside the tile
-    const int64_t tiles_per_mat = row_tiles * col_tiles;
-    int buf = 0;
-    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, buf ^= 1) {
-        const int64_t bt = t / tiles_per_mat;
-        const int64_t rem = t - bt * tiles_per_mat;
-        const int64_t rt = rem / col_tiles;
-        const int64_t ct = rem - rt * col_tiles;
+    const int64_t total_tiles = g.tile_start[g.count];
+
+    if (tid == 0) {
+        for (int s = 0; s < kMxStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    auto issue = [&](int64_t t, int s) {          // thread 0 only
+        const int gi = group_of(g, t);
+        const int64_t local = t - g.tile_start[gi];
+        const int64_t bt = local / g.tiles_per_mat[gi];
+        const int64_t rem = local - bt * g.tiles_per_mat[gi];
+        const int64_t rt = rem / g.col_tiles[gi];
+        const int64_t ct = rem - rt * g.col_tiles[gi];
+        mbar_arrive_expect_tx(&full[s], kMxStageBytes);
+        tma_2d_g2s(smem + (size_t)s * kMxStageBytes, &g.tmap[gi], (int)(ct * 128), (int)(bt * g.m[gi] + rt * 128),
+                   &full[s]);
+    };
+    if (tid == 0)
+        for (int s = 0; s < kMxStages; ++s) {
+            const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+            if (t < total_tiles) issue(t, s);
+        }
+
+    int it = 0;
+    bool failed = false;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const int s = it % kMxStages;
+        const bool ok = mbar_wait(&full[s], (uint32_t)(it / kMxStages) & 1u);
+        const uint8_t* st = smem + (size_t)s * kMxStageBytes;
+        uint8_t* sb = sbuf + (it & 1) * 512;
+        const int gi = group_of(g, t);
+        const int64_t m = g.m[gi], k = g.k[gi];
+        const int64_t local = t - g.tile_start[gi];
+        const int64_t bt = local / g.tiles_per_mat[gi];
+        const int64_t rem = local - bt * g.tiles_per_mat[gi];
+        const int64_t rt = rem / g.col_tiles[gi];
+        const int64_t ct = rem - rt * g.col_tiles[gi];
         const int64_t col = ct * 128 + c * 8;
         const bool col_ok = col < k;
-        uint4 v[8];
+        uint8_t* codes = g.codes[gi];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int64_t row = rt * 128 + warp * kMxRowsPerWarp + 2 * i + (lane >> 4);
-            v[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (col_ok && row < m) v[i] = ld_stream(w + ((bt * m + row) * k + col));
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kMxRowsPerWarp / 2; ++i) {
             const int rl = warp * kMxRowsPerWarp + 2 * i + (lane >> 4);    // row inside the tile
             const int64_t row = rt * 128 + rl;
+            const uint4 v = *reinterpret_cast<const uint4*>(st + rl * 256 + c * 16);
             float f[8];
-            unpack8(v[i], f);
+            unpack8(v, f);
             float a = fabsf(f[0]);
 #pragma unroll
             for (int e = 1; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
             a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
             const int E = (int)(__float_as_uint(a) >> 23);           // a >= 0: no sign bit
-            const int e8 = E > 8 ? E - 8 : 0;                          // E8M0 byte
+            const bool valid = col_ok && row < m;
+            const int e8 = (valid && E > 8) ? E - 8 : 0;              // E8M0 byte; padding stays 0
             const float factor = __uint_as_float((uint32_t)(254 - e8) << 23);   // 2^(127 - e8)
             float q[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) q[e] = __fmul_rn(f[e], factor);
-            if (col_ok && row < m)
+            if (valid)
                 st_stream(codes + ((bt * m + row) * k + col),
                           make_uint2(cvt_fp8x4<kE4M3>(q[0], q[1], q[2], q[3]), cvt_fp8x4<kE4M3>(q[4], q[5], q[6], q[7])));
-            if ((c & 3u) == 0)   // padded rows / columns keep e8 == 0
-                sbuf[buf][(rl & 31) * 16 + (rl >> 5) * 4 + jl] = (uint8_t)e8;
+            if ((c & 3u) == 0) sb[(rl & 31) * 16 + (rl >> 5) * 4 + jl] = (uint8_t)e8;
         }
-        __syncthreads();
-        if (threadIdx.x < 32)
-            st_stream(scales + t * 512 + threadIdx.x * 16, *reinterpret_cast<const uint4*>(&sbuf[buf][threadIdx.x * 16]));
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0) {
+            const int64_t tn = t + (int64_t)kMxStages * gridDim.x;
+            if (tn < total_tiles) {
+                fence_proxy_async_smem();
+                issue(tn, s);
+            }
+        }
+        if (tid < 32) st_stream(g.scales[gi] + local * 512 + tid * 16, *reinterpret_cast<const uint4*>(sb + tid * 16));
+    }
+    if (failed && tid == 0) {
+        raise_error(kErrCopyTimeout);
+        for (int jj = it; jj < it + kMxStages; ++jj) {
+            const int64_t tj = blockIdx.x + (int64_t)jj * gridDim.x;
+            if (tj < total_tiles) mbar_wait(&full[jj % kMxStages], (uint32_t)(jj / kMxStages) & 1u);
+        }
     }
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link the driver library directly).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace fp8q
+
+namespace fp8q {
+unsigned unit_errors_mxfp8(bool clear) { return read_unit_errors(clear); }
 }  // namespace fp8q
 
 using namespace fp8q;
@@ -92,25 +195,113 @@ extern "C" size_t mxfp8_swizzled_scale_bytes(int64_t batch, int64_t m, int64_t k
     return (size_t)batch * (size_t)((m + 127) / 128) * (size_t)((kb + 3) / 4) * 512u;
 }
 
+namespace fp8q {
+
+// Argument checks of one tensor of a group; sets *tiles to its tile count.
+static fp8q_status_t check_tensor(const mxfp8_tensor_t& t, int64_t* tiles) {
+    *tiles = 0;
+    if (t.batch < 0 || t.m < 0) return FP8Q_ERR_SIZE;
+    if (t.k <= 0 || t.k % MXFP8_BLOCK != 0) return FP8Q_ERR_K;
+    if (t.m > 0 && t.batch > 0 && (uint64_t)t.k > FP8Q_MAX_ELEMENTS / (uint64_t)t.m / (uint64_t)t.batch)
+        return FP8Q_ERR_SIZE;
+    const size_t n = (size_t)t.batch * (size_t)t.m * (size_t)t.k;
+    if (n == 0) return FP8Q_OK;
+    if (!t.w_bf16 || !t.codes || !t.scales_swizzled) return FP8Q_ERR_NULL;
+    if (!aligned16(t.w_bf16) || !aligned16(t.codes) || !aligned16(t.scales_swizzled)) return FP8Q_ERR_ALIGN;
+    // tensor-map coordinates are 32-bit signed
+    if (t.batch * t.m >= (int64_t)1 << 31 || t.k >= (int64_t)1 << 31) return FP8Q_ERR_SIZE;
+    *tiles = t.batch * ((t.m + 127) / 128) * ((t.k / MXFP8_BLOCK + 3) / 4);
+    return FP8Q_OK;
+}
+
+// The byte ranges a tensor reads (0) and writes (1, 2).
+static void tensor_ranges(const mxfp8_tensor_t& t, const void* p[3], size_t sz[3]) {
+    const size_t n = (size_t)t.batch * (size_t)t.m * (size_t)t.k;
+    p[0] = t.w_bf16;
+    sz[0] = 2 * n;
+    p[1] = t.codes;
+    sz[1] = n;
+    p[2] = t.scales_swizzled;
+    sz[2] = mxfp8_swizzled_scale_bytes(t.batch, t.m, t.k);
+}
+
+static fp8q_status_t launch_group(const mxfp8_tensor_t* tensors, int count, cudaStream_t stream) {
+    if (!tensors) return FP8Q_ERR_NULL;
+    if (count < 1 || count > kMxMaxGroup) return FP8Q_ERR_SIZE;
+    int64_t tiles[kMxMaxGroup];
+    for (int i = 0; i < count; ++i) {
+        const fp8q_status_t st = check_tensor(tensors[i], &tiles[i]);
+        if (st != FP8Q_OK) return st;
+    }
+    // no output may overlap any input or output of any tensor of the group
+    for (int i = 0; i < count; ++i) {
+        if (tiles[i] == 0) continue;
+        const void* pi[3];
+        size_t si[3];
+        tensor_ranges(tensors[i], pi, si);
+        for (int j = 0; j < count; ++j) {
+            if (tiles[j] == 0) continue;
+            const void* pj[3];
+            size_t sj[3];
+            tensor_ranges(tensors[j], pj, sj);
+            for (int a = 1; a < 3; ++a)
+                for (int b = 0; b < 3; ++b) {
+                    if (i == j && a == b) continue;
+                    if (overlaps(pi[a], si[a], pj[b], sj[b])) return FP8Q_ERR_ALIAS;
+                }
+        }
+    }
+    int64_t all_tiles = 0;
+    for (int i = 0; i < count; ++i) all_tiles += tiles[i];
+    if (all_tiles == 0) return FP8Q_OK;                 // nothing to do, nothing launched
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cuda_status(cudaErrorNotSupported);
+    MxGroup g;
+    int used = 0;
+    int64_t start = 0;
+    for (int i = 0; i < count; ++i) {
+        const mxfp8_tensor_t& t = tensors[i];
+        if (tiles[i] == 0) continue;
+        // the weights as a 2D [batch * m, k] array of 16-bit elements, 128 x 128 boxes
+        const cuuint64_t dims[2] = {(cuuint64_t)t.k, (cuuint64_t)(t.batch * t.m)};
+        const cuuint64_t strides[1] = {(cuuint64_t)t.k * 2};
+        const cuuint32_t box[2] = {128, 128};
+        const cuuint32_t estride[2] = {1, 1};
+        const CUresult cr = encode(&g.tmap[used], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(t.w_bf16), dims,
+                                   strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cuda_status(cudaErrorInvalidValue);
+        g.m[used] = t.m;
+        g.k[used] = t.k;
+        g.col_tiles[used] = (t.k / MXFP8_BLOCK + 3) / 4;
+        g.tiles_per_mat[used] = ((t.m + 127) / 128) * g.col_tiles[used];
+        g.tile_start[used] = start;
+        g.codes[used] = t.codes;
+        g.scales[used] = t.scales_swizzled;
+        start += tiles[i];
+        ++used;
+    }
+    if (used == 0) return FP8Q_OK;
+    g.tile_start[used] = start;
+    g.count = used;
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(mxfp8_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMxSmem);
+    if (attr != cudaSuccess) return cuda_status(attr);
+    static int resident = resident_blocks(mxfp8_quantize_kernel, kMxThreads, kMxSmem);
+    const unsigned grid = grid_for((size_t)start, resident);
+    mxfp8_quantize_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(g);
+    return launch_status();
+}
+
+}  // namespace fp8q
+
 extern "C" fp8q_status_t mxfp8_quantize_swizzled(const void* w_bf16, int64_t batch, int64_t m, int64_t k,
                                                  uint8_t* codes, uint8_t* scales_swizzled, fp8q_stream_t stream) {
-    if (batch < 0 || m < 0) return FP8Q_ERR_SIZE;
-    if (k <= 0 || k % MXFP8_BLOCK != 0) return FP8Q_ERR_K;
-    if (m > 0 && batch > 0 && (uint64_t)k > FP8Q_MAX_ELEMENTS / (uint64_t)m / (uint64_t)batch) return FP8Q_ERR_SIZE;
-    const size_t n = (size_t)batch * (size_t)m * (size_t)k;
-    if (n == 0) return FP8Q_OK;
-    if (!w_bf16 || !codes || !scales_swizzled) return FP8Q_ERR_NULL;
-    if (!aligned16(w_bf16) || !aligned16(codes) || !aligned16(scales_swizzled)) return FP8Q_ERR_ALIGN;
-    const size_t sbytes = mxfp8_swizzled_scale_bytes(batch, m, k);
-    if (overlaps(codes, n, w_bf16, 2 * n) || overlaps(scales_swizzled, sbytes, w_bf16, 2 * n) ||
-        overlaps(codes, n, scales_swizzled, sbytes))
-        return FP8Q_ERR_ALIAS;
-    static int resident = resident_blocks(mxfp8_quantize_kernel, kMxThreads);
-    const int64_t row_tiles = (m + 127) / 128;
-    const int64_t col_tiles = (k / MXFP8_BLOCK + 3) / 4;
-    const int64_t total = batch * row_tiles * col_tiles;
-    const unsigned grid = grid_for((size_t)total, resident);
-    mxfp8_quantize_kernel<<<grid, kMxThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(w_bf16), m, k, row_tiles, col_tiles, total, codes, scales_swizzled);
-    return launch_status();
+    const mxfp8_tensor_t t = {w_bf16, batch, m, k, codes, scales_swizzled};
+    return launch_group(&t, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8q_status_t mxfp8_quantize_swizzled_group(const mxfp8_tensor_t* tensors, int count,
+                                                       fp8q_stream_t stream) {
+    return launch_group(tensors, count, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -1,0 +1,140 @@
+// The receiving side of a prequantized MXFP8 transfer.
+//
+// "perf: Reduce MXFP8 refit weight-transfer overheads": the receiver loads
+// the E4M3 weights with their *_scale_from_checkpoint (Safety), rearranges
+// scales for its GEMMs (the "MXFP8 shuffle", whose result is checked
+// bit-exactly by NRL_MXFP8_SHUFFLE_VERIFY in the 30B / 235B reproductions)
+// and, in the review of the sm100 fast path, expects scales shaped
+// [M, K/32].  Three small kernels serve that side:
+//   mxfp8_dequantize_swizzled  w = RNE_bf16(decode_e4m3(c) * 2^(e - 127))
+//   mxfp8_unswizzle_scales     swizzled E8M0 bytes -> row-major [batch, m, k/32]
+//   fp8q_count_mismatches      number of differing bytes of two buffers
+// None of them is on the sender's hot path; they are grid-stride kernels with
+// 16-byte accesses.
+#include "fp8q_device.cuh"
+#include "fp8q_host.cuh"
+
+namespace fp8q {
+
+__device__ __forceinline__ int64_t swizzle_offset(int64_t bt, int64_t r, int64_t j, int64_t m, int64_t kb) {
+    const int64_t col_tiles = (kb + 3) / 4, row_tiles = (m + 127) / 128;
+    return bt * row_tiles * col_tiles * 512 + ((r / 128) * col_tiles + j / 4) * 512 + (r % 32) * 16 +
+           ((r % 128) / 32) * 4 + (j % 4);
+}
+
+// One thread per 16 consecutive codes (half of a 32-element block).
+__global__ void __launch_bounds__(256)
+mxfp8_dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int64_t m,
+                        int64_t k, size_t units, uint16_t* __restrict__ out) {
+    const int64_t kb = k / 32;
+    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (size_t)gridDim.x * blockDim.x) {
+        const size_t e0 = u * 16;
+        const int64_t row = (int64_t)(e0 / (size_t)k);        // row of the [batch * m, k] view
+        const int64_t col = (int64_t)(e0 - (size_t)row * (size_t)k);
+        const int64_t bt = row / m, r = row - bt * m;
+        const uint32_t e8 = scales[swizzle_offset(bt, r, col / 32, m, kb)];
+        // 2^(e8 - 127): a normal binary32 for e8 >= 1, the subnormal 2^-127 for e8 == 0
+        const float factor = __uint_as_float(e8 ? (e8 << 23) : 0x00400000u);
+        const uint4 c = ld_stream(codes + e0);
+        float d[16];
+        decode_fp8x4<kE4M3>(c.x, d);
+        decode_fp8x4<kE4M3>(c.y, d + 4);
+        decode_fp8x4<kE4M3>(c.z, d + 8);
+        decode_fp8x4<kE4M3>(c.w, d + 12);
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)     // the products are exact; only the bf16 rounding rounds
+            h[i] = pack_bf16x2(__fmul_rn(d[2 * i], factor), __fmul_rn(d[2 * i + 1], factor));
+        st_stream(out + e0, make_uint4(h[0], h[1], h[2], h[3]));
+        st_stream(out + e0 + 8, make_uint4(h[4], h[5], h[6], h[7]));
+    }
+}
+
+__global__ void __launch_bounds__(256)
+mxfp8_unswizzle_kernel(const uint8_t* __restrict__ scales, int64_t m, int64_t kb, size_t total,
+                       uint8_t* __restrict__ out) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int64_t j = (int64_t)(i % (size_t)kb);
+        const int64_t row = (int64_t)(i / (size_t)kb);
+        const int64_t bt = row / m, r = row - bt * m;
+        out[i] = scales[swizzle_offset(bt, r, j, m, kb)];
+    }
+}
+
+// Adds the number of differing bytes of a and b to *count.
+__global__ void __launch_bounds__(256)
+count_mismatches_kernel(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b, size_t n,
+                        unsigned long long* count) {
+    unsigned long long mine = 0;
+    const size_t n16 = n / 16;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (size_t i = t0; i < n16; i += stride) {
+        const uint4 x = ld_stream(a + 16 * i), y = ld_stream(b + 16 * i);
+        // __vcmpne4: 0xFF in every byte lane that differs
+        mine += __popc(__vcmpne4(x.x, y.x)) / 8 + __popc(__vcmpne4(x.y, y.y)) / 8 +
+                __popc(__vcmpne4(x.z, y.z)) / 8 + __popc(__vcmpne4(x.w, y.w)) / 8;
+    }
+    for (size_t i = 16 * n16 + t0; i < n; i += stride) mine += a[i] != b[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xFFFFFFFFu, mine, o);
+    if ((threadIdx.x & 31u) == 0 && mine) atomicAdd(count, mine);
+}
+
+static fp8q_status_t check_mx_shape(int64_t batch, int64_t m, int64_t k) {
+    if (batch < 0 || m < 0) return FP8Q_ERR_SIZE;
+    if (k <= 0 || k % MXFP8_BLOCK != 0) return FP8Q_ERR_K;
+    if (m > 0 && batch > 0 && (uint64_t)k > FP8Q_MAX_ELEMENTS / (uint64_t)m / (uint64_t)batch) return FP8Q_ERR_SIZE;
+    return FP8Q_OK;
+}
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" fp8q_status_t mxfp8_dequantize_swizzled(const uint8_t* codes, const uint8_t* scales_swizzled, int64_t batch,
+                                                   int64_t m, int64_t k, void* out_bf16, fp8q_stream_t stream) {
+    fp8q_status_t st = check_mx_shape(batch, m, k);
+    if (st != FP8Q_OK) return st;
+    const size_t n = (size_t)batch * (size_t)m * (size_t)k;
+    if (n == 0) return FP8Q_OK;
+    if (!codes || !scales_swizzled || !out_bf16) return FP8Q_ERR_NULL;
+    if (!aligned16(codes) || !aligned16(scales_swizzled) || !aligned16(out_bf16)) return FP8Q_ERR_ALIGN;
+    const size_t sb = mxfp8_swizzled_scale_bytes(batch, m, k);
+    if (overlaps(out_bf16, 2 * n, codes, n) || overlaps(out_bf16, 2 * n, scales_swizzled, sb)) return FP8Q_ERR_ALIAS;
+    static int resident = resident_blocks(mxfp8_dequantize_kernel, 256);
+    const size_t units = n / 16;
+    mxfp8_dequantize_kernel<<<grid_for((units + 255) / 256, resident), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        codes, scales_swizzled, m, k, units, static_cast<uint16_t*>(out_bf16));
+    return launch_status();
+}
+
+extern "C" fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, int64_t batch, int64_t m, int64_t k,
+                                                uint8_t* scales_rowmajor, fp8q_stream_t stream) {
+    fp8q_status_t st = check_mx_shape(batch, m, k);
+    if (st != FP8Q_OK) return st;
+    const size_t total = (size_t)batch * (size_t)m * (size_t)(k / MXFP8_BLOCK);
+    if (total == 0) return FP8Q_OK;
+    if (!scales_swizzled || !scales_rowmajor) return FP8Q_ERR_NULL;
+    if (!aligned16(scales_swizzled) || !aligned16(scales_rowmajor)) return FP8Q_ERR_ALIGN;
+    if (overlaps(scales_rowmajor, total, scales_swizzled, mxfp8_swizzled_scale_bytes(batch, m, k)))
+        return FP8Q_ERR_ALIAS;
+    static int resident = resident_blocks(mxfp8_unswizzle_kernel, 256);
+    mxfp8_unswizzle_kernel<<<grid_for((total + 255) / 256, resident), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        scales_swizzled, m, k / MXFP8_BLOCK, total, scales_rowmajor);
+    return launch_status();
+}
+
+extern "C" fp8q_status_t fp8q_count_mismatches(const void* a, const void* b, size_t nbytes, unsigned long long* count,
+                                               fp8q_stream_t stream) {
+    if (nbytes > 16 * FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
+    if (nbytes == 0) return FP8Q_OK;
+    if (!a || !b || !count) return FP8Q_ERR_NULL;
+    if (!aligned16(a) || !aligned16(b) || (reinterpret_cast<uintptr_t>(count) & 7u)) return FP8Q_ERR_ALIGN;
+    if (overlaps(count, 8, a, nbytes) || overlaps(count, 8, b, nbytes)) return FP8Q_ERR_ALIAS;
+    static int resident = resident_blocks(count_mismatches_kernel, 256);
+    count_mismatches_kernel<<<grid_for((nbytes / 16 + 255) / 256 + 1, resident), 256, 0,
+                              reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<const uint8_t*>(a),
+                                                                         static_cast<const uint8_t*>(b), nbytes, count);
+    return launch_status();
+}

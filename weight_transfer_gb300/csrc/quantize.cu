@@ -5,78 +5,132 @@
 // one fp32 scale per 128-element block, scale = amax / Fmax, codes are the
 // satfinite round-to-nearest-even conversion of x / scale.
 //
-// Work split: 8 lanes own one 128-element block; lane j holds elements
-// [8j, 8j+8) and [64+8j, 64+8j+8), so each of the two 16-byte load
-// instructions of a warp reads four whole 128-byte half-blocks.  A warp covers
-// 4 blocks per step and U steps are loaded before any is processed (2U
-// independent 16-byte loads in flight per lane).  The block amax is a 3-step
-// xor-shuffle inside the 8-lane group; the quotients x / s use the per-block
-// reciprocal with one Markstein correction (exact for bf16 dividends, see
-// block_quotients).  The grid is persistent (SM count x resident blocks).
+// Work split: a persistent CTA of 256 threads walks tiles of 64 blocks
+// (8192 elements, 16 KB of bf16).  Thread 0 keeps up to kQuantStages tiles
+// in flight, each one bulk copy (cp.async.bulk) into a shared-memory stage
+// armed on that stage's mbarrier, so the loads in flight are not bounded by
+// registers.  Once a stage has landed, 8 lanes own one block: lane j reads
+// elements [8j, 8j+8) and [64+8j, 64+8j+8) from shared memory (each 8-lane
+// phase reads 128 contiguous bytes, no bank conflicts), a warp covers 4
+// blocks per round, the CTA 32 blocks per round, 2 rounds per tile.  The
+// block amax is a 3-step xor-shuffle inside the 8-lane group; the quotients
+// x / s use the per-block reciprocal with one Markstein correction (exact for
+// bf16 dividends, see block_quotients).  The ragged last tile (n not a
+// multiple of 8192) is read straight from global memory.
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
 namespace fp8q {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantUnroll = 2;
+constexpr int kQuantTileBlocks = 64;
+constexpr int kQuantTile = kQuantTileBlocks * 128;        // elements
+constexpr int kQuantStageBytes = kQuantTile * 2;
+constexpr int kQuantStages = 3;
+constexpr size_t kQuantSmem = (size_t)kQuantStages * kQuantStageBytes + 8 * kQuantStages;
 
-template <int FMT, int U>
+// One block's worth of work for one lane: 16 bf16 in two 8-element halves
+// (va, vb) -> amax over the 8-lane group, scale, 16 codes.
+template <int FMT>
+__device__ __forceinline__ void quantize_block16(const uint4& va, const uint4& vb, uint32_t (&wa)[2],
+                                                 uint32_t (&wb)[2], float& scale) {
+    float f[16];
+    unpack8(va, *reinterpret_cast<float(*)[8]>(f));
+    unpack8(vb, *reinterpret_cast<float(*)[8]>(f + 8));
+    float a = fabsf(f[0]);
+#pragma unroll
+    for (int i = 1; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+    const float s = block_scale<FMT>(a);
+    float q[16];
+    block_quotients<1, 16>(f, s, q);
+    wa[0] = cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]);
+    wa[1] = cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7]);
+    wb[0] = cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]);
+    wb[1] = cvt_fp8x4<FMT>(q[12], q[13], q[14], q[15]);
+    scale = s;
+}
+
+template <int FMT>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_blockwise_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __restrict__ codes,
                           float* __restrict__ scales) {
-    const size_t nb = (n + 127) >> 7;       // blocks, the last one possibly partial
-    const size_t nfull = n >> 7;            // full blocks
-    const unsigned lane = threadIdx.x & 31u;
-    const unsigned j = lane & 7u;           // lane inside the block's 8-lane group
-    const unsigned sub = lane >> 3;         // which of the warp's 4 blocks
-    const size_t warp = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuantStages * kQuantStageBytes);
+    const size_t nb = (n + 127) >> 7;
+    const size_t ntiles = (n + kQuantTile - 1) / kQuantTile;
+    const size_t nstaged = n / kQuantTile;                // tiles entirely inside the array
+    const unsigned tid = threadIdx.x;
+    const unsigned lane = tid & 31u, warp = tid >> 5;
+    const unsigned j = lane & 7u, sub = lane >> 3;
 
-    // the loop bound is warp-uniform so every shuffle below has all 32 lanes
-    for (size_t base = warp; 4 * base < nb; base += nwarps * U) {
-        uint4 va[U], vb[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const size_t b = 4 * (base + (size_t)u * nwarps) + sub;
-            const size_t e0 = (b << 7) + 8 * j;
-            if (b < nfull) {
-                va[u] = ld_stream(x + e0);
-                vb[u] = ld_stream(x + e0 + 64);
-            } else if (b < nb) {
-                va[u] = ld_bf16x8_tail(x + e0, (long long)n - (long long)e0);
-                vb[u] = ld_bf16x8_tail(x + e0 + 64, (long long)n - (long long)e0 - 64);
-            } else {
-                va[u] = make_uint4(0u, 0u, 0u, 0u);
-                vb[u] = va[u];
-            }
+    if (tid == 0) {
+        for (int s = 0; s < kQuantStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    auto issue = [&](size_t t, int s) {           // thread 0 only
+        mbar_arrive_expect_tx(&full[s], kQuantStageBytes);
+        bulk_g2s(smem + (size_t)s * kQuantStageBytes, x + t * kQuantTile, kQuantStageBytes, &full[s]);
+    };
+    if (tid == 0)
+        for (int s = 0; s < kQuantStages; ++s) {
+            const size_t t = blockIdx.x + (size_t)s * gridDim.x;
+            if (t < nstaged) issue(t, s);
         }
+
+    int it = 0;
+    bool failed = false;
+    for (size_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = it % kQuantStages;
+        const bool staged = t < nstaged;
+        const bool ok = staged ? mbar_wait(&full[s], (uint32_t)(it / kQuantStages) & 1u) : true;
+        const uint8_t* st = smem + (size_t)s * kQuantStageBytes;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const size_t b = 4 * (base + (size_t)u * nwarps) + sub;
+        for (int m = 0; m < kQuantTileBlocks / 32; ++m) {
+            const unsigned bl = m * 32 + warp * 4 + sub;          // block inside the tile
+            const size_t b = t * kQuantTileBlocks + bl;            // block inside the array
             const size_t e0 = (b << 7) + 8 * j;
-            float f[16];
-            unpack8(va[u], *reinterpret_cast<float(*)[8]>(f));
-            unpack8(vb[u], *reinterpret_cast<float(*)[8]>(f + 8));
-            float a = fabsf(f[0]);
-#pragma unroll
-            for (int i = 1; i < 16; ++i) a = fmaxf(a, fabsf(f[i]));
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-            const float s = block_scale<FMT>(a);
-            float q[16];
-            block_quotients<1, 16>(f, s, q);
-            uint32_t wa[2] = {cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])};
-            uint32_t wb[2] = {cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]), cvt_fp8x4<FMT>(q[12], q[13], q[14], q[15])};
-            if (b < nfull) {
+            uint4 va, vb;
+            if (staged) {
+                va = *reinterpret_cast<const uint4*>(st + bl * 256 + j * 16);
+                vb = *reinterpret_cast<const uint4*>(st + bl * 256 + 128 + j * 16);
+            } else {
+                va = ld_bf16x8_tail(x + e0, (long long)n - (long long)e0);
+                vb = ld_bf16x8_tail(x + e0 + 64, (long long)n - (long long)e0 - 64);
+            }
+            uint32_t wa[2], wb[2];
+            float sc;
+            quantize_block16<FMT>(va, vb, wa, wb, sc);
+            if (staged) {
                 st_stream(codes + e0, make_uint2(wa[0], wa[1]));
                 st_stream(codes + e0 + 64, make_uint2(wb[0], wb[1]));
+                if (j == 0) scales[b] = sc;
             } else if (b < nb) {
                 st_u8_tail(codes + e0, wa, 2, (long long)n - (long long)e0);
                 st_u8_tail(codes + e0 + 64, wb, 2, (long long)n - (long long)e0 - 64);
+                if (j == 0) scales[b] = sc;
             }
-            if (b < nb && j == 0) scales[b] = s;
+        }
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0) {
+            const size_t tn = t + (size_t)kQuantStages * gridDim.x;
+            if (tn < nstaged) {
+                fence_proxy_async_smem();
+                issue(tn, s);
+            }
+        }
+    }
+    if (failed && tid == 0) {
+        raise_error(kErrCopyTimeout);
+        for (int jj = it; jj < it + kQuantStages; ++jj) {
+            const size_t tj = blockIdx.x + (size_t)jj * gridDim.x;
+            if (tj < nstaged) mbar_wait(&full[jj % kQuantStages], (uint32_t)(jj / kQuantStages) & 1u);
         }
     }
 }
@@ -103,11 +157,13 @@ encode_f32_kernel(const float* __restrict__ x, size_t n, uint8_t* __restrict__ c
 template <int FMT>
 static fp8q_status_t launch_quantize(const uint16_t* x, size_t n, uint8_t* codes, float* scales,
                                      cudaStream_t stream) {
-    static int resident = resident_blocks(quantize_blockwise_kernel<FMT, kQuantUnroll>, kQuantThreads);
-    const size_t nb = (n + 127) / 128;
-    const size_t blocks_per_cta = (kQuantThreads / 8) * kQuantUnroll;
-    const unsigned grid = grid_for((nb + blocks_per_cta - 1) / blocks_per_cta, resident);
-    quantize_blockwise_kernel<FMT, kQuantUnroll><<<grid, kQuantThreads, 0, stream>>>(x, n, codes, scales);
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        quantize_blockwise_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQuantSmem);
+    if (attr != cudaSuccess) return cuda_status(attr);
+    static int resident = resident_blocks(quantize_blockwise_kernel<FMT>, kQuantThreads, kQuantSmem);
+    const size_t tiles = (n + kQuantTile - 1) / kQuantTile;
+    const unsigned grid = grid_for(tiles, resident);
+    quantize_blockwise_kernel<FMT><<<grid, kQuantThreads, kQuantSmem, stream>>>(x, n, codes, scales);
     return launch_status();
 }
 
@@ -120,6 +176,10 @@ static fp8q_status_t launch_encode(const float* x, size_t n, uint8_t* codes, cud
     return launch_status();
 }
 
+}  // namespace fp8q
+
+namespace fp8q {
+unsigned unit_errors_quantize(bool clear) { return read_unit_errors(clear); }
 }  // namespace fp8q
 
 using namespace fp8q;

@@ -6,12 +6,18 @@
 // every shard to HBM and reduces afterwards; the fused kernel reads each
 // shard's codes and scales once and keeps the running sum in registers.
 //
-// Work split: a lane owns 16 consecutive elements (one 16-byte load of codes
-// per shard), 8 lanes cover one 128-element block.  All k shard loads of a
-// lane are issued before the first is decoded (k independent 16-byte loads
-// in flight per lane), then the sum runs in rank order 0..k-1:
+// Work split: a persistent CTA of 512 threads walks tiles of 4096 elements
+// (32 blocks).  Thread 0 keeps up to kRedStages tiles in flight: for each
+// tile it issues 2k bulk copies (the k shards' 4096 codes and 32 scales)
+// into one shared-memory stage, armed on that stage's mbarrier.  All threads
+// wait on the stage's barrier, then each takes 4 consecutive elements in
+// each of 2 rounds (a warp covers 128 contiguous elements, one block, per
+// round), reads its codes and the block's scale from shared memory and sums
+// in rank order 0..k-1:
 //   acc = +0;  acc = RN(acc + RN(decode(c_r) * s_r))
-// with explicit _rn intrinsics so nothing is fused into an FMA.
+// with explicit _rn intrinsics so nothing is fused into an FMA.  Each round
+// a warp stores 512 contiguous bytes of fp32 and 256 of bf16.  The ragged
+// last tile (n not a multiple of 4096) is read straight from global memory.
 #include <mutex>
 
 #include "fp8q_device.cuh"
@@ -19,14 +25,30 @@
 
 namespace fp8q {
 
-constexpr int kRedThreads = 256;
+constexpr int kRedThreads = 512;
+constexpr int kRedTile = 4096;
+constexpr int kRedStages = 3;
+
+// Shared memory of one stage for k shards: k x (4096 codes + 32 fp32 scales).
+__host__ __device__ constexpr uint32_t red_stage_bytes(int k) { return (uint32_t)k * (kRedTile + 4 * (kRedTile / 128)); }
+constexpr size_t red_smem_bytes(int k) { return (size_t)kRedStages * red_stage_bytes(k) + 8 * kRedStages; }
 
 struct ShardPtrs {
     const uint8_t* codes[FP8Q_MAX_SHARDS];
     const float* scales[FP8Q_MAX_SHARDS];
 };
 
-// Writes 16 results: fp32 as four 16-byte stores, bf16 as two.
+// 4 results at element e: fp32 as one 16-byte store, bf16 as one 8-byte store.
+template <bool OUT_BF16, bool OUT_F32>
+__device__ __forceinline__ void store4(const float (&acc)[4], size_t e, uint16_t* out_bf16, float* out_f32) {
+    if (OUT_F32)
+        st_stream(out_f32 + e, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                                          __float_as_uint(acc[3])));
+    if (OUT_BF16) st_stream(out_bf16 + e, make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3])));
+}
+
+// 16 results at element e0 (the comparator's second pass): fp32 as four
+// 16-byte stores, bf16 as two; a ragged end element by element.
 template <bool OUT_BF16, bool OUT_F32>
 __device__ __forceinline__ void store16(const float (&acc)[16], size_t e0, size_t n, uint16_t* out_bf16,
                                         float* out_f32) {
@@ -57,43 +79,118 @@ __device__ __forceinline__ void store16(const float (&acc)[16], size_t e0, size_
 
 // SUM = true: acc starts at +0 and every shard is added (the reduce).
 // SUM = false: k == 1 and the dequantized value is written as is (dequantize).
-template <int FMT, bool OUT_BF16, bool OUT_F32, bool SUM>
+// KMAX >= k bounds the unrolled shard loop (a power of two, so at most half
+// of the unrolled iterations are switched off).
+template <int FMT, bool OUT_BF16, bool OUT_F32, bool SUM, int KMAX>
 __global__ void __launch_bounds__(kRedThreads)
 dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32) {
-    const size_t units = (n + 15) >> 4;
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
-        const size_t e0 = u << 4;
-        const size_t b = u >> 3;
-        const bool full = e0 + 16 <= n;
-        uint4 cv[FP8Q_MAX_SHARDS];
-        float sv[FP8Q_MAX_SHARDS];
-#pragma unroll
-        for (int r = 0; r < FP8Q_MAX_SHARDS; ++r) {
-            if (r < k) {
-                cv[r] = full ? ld_stream(sh.codes[r] + e0) : ld_u8x16_tail(sh.codes[r] + e0, (long long)n - (long long)e0);
-                sv[r] = ld_stream_f32(sh.scales[r] + b);
-            }
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t stage_bytes = red_stage_bytes(k);
+    const uint32_t codes_bytes = (uint32_t)k * kRedTile;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRedStages * stage_bytes);
+    const size_t ntiles = (n + kRedTile - 1) / kRedTile;
+    const size_t nstaged = n / kRedTile;               // tiles entirely inside the arrays
+    const unsigned tid = threadIdx.x;
+
+    if (tid == 0) {
+        for (int s = 0; s < kRedStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](size_t t, int s) {           // thread 0 only
+        uint8_t* st = smem + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        for (int r = 0; r < k; ++r) {
+            bulk_g2s(st + r * kRedTile, sh.codes[r] + t * kRedTile, kRedTile, &full[s]);
+            bulk_g2s(st + codes_bytes + r * (4 * kRedTile / 128), sh.scales[r] + t * (kRedTile / 128),
+                     4 * kRedTile / 128, &full[s]);
         }
-        float acc[16];
+    };
+    if (tid == 0)
+        for (int s = 0; s < kRedStages; ++s) {
+            const size_t t = blockIdx.x + (size_t)s * gridDim.x;
+            if (t < nstaged) issue(t, s);
+        }
+
+    int it = 0;
+    bool failed = false;
+    for (size_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = it % kRedStages;
+        const bool staged = t < nstaged;
+        const bool ok = staged ? mbar_wait(&full[s], (uint32_t)(it / kRedStages) & 1u) : true;
+        const uint8_t* st = smem + (size_t)s * stage_bytes;
+#pragma unroll 1
+        for (int m = 0; m < kRedTile / (4 * kRedThreads); ++m) {
+            const uint32_t el = m * (4 * kRedThreads) + 4 * tid;   // element inside the tile
+            const size_t e = t * kRedTile + el;               // element inside the arrays
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (staged) {
+                uint32_t w[KMAX];
+                float sc[KMAX];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+                for (int r = 0; r < KMAX; ++r) {
+                    if (r < k) {
+                        w[r] = *reinterpret_cast<const uint32_t*>(st + r * kRedTile + el);
+                        sc[r] = *reinterpret_cast<const float*>(st + codes_bytes + r * (4 * kRedTile / 128) +
+                                                                (el >> 7) * 4);
+                    }
+                }
 #pragma unroll
-        for (int r = 0; r < FP8Q_MAX_SHARDS; ++r) {
-            if (r < k) {
-                float d[16];
-                decode_fp8x4<FMT>(cv[r].x, d);
-                decode_fp8x4<FMT>(cv[r].y, d + 4);
-                decode_fp8x4<FMT>(cv[r].z, d + 8);
-                decode_fp8x4<FMT>(cv[r].w, d + 12);
+                for (int r = 0; r < KMAX; ++r) {
+                    if (r < k) {
+                        float d[4];
+                        decode_fp8x4<FMT>(w[r], d);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p = __fmul_rn(d[i], sv[r]);
-                    acc[i] = SUM ? __fadd_rn(acc[i], p) : p;
+                        for (int q = 0; q < 4; ++q) {
+                            const float p = __fmul_rn(d[q], sc[r]);
+                            acc[q] = SUM ? __fadd_rn(acc[q], p) : p;
+                        }
+                    }
+                }
+                store4<OUT_BF16, OUT_F32>(acc, e, out_bf16, out_f32);
+            } else if (e < n) {
+                // the ragged last tile, element by element from global memory
+                for (int r = 0; r < k; ++r) {
+                    const float sc = sh.scales[r][e >> 7];
+                    for (int q = 0; q < 4; ++q) {
+                        if (e + q < n) {
+                            const float d = decode_fp8x2<FMT>(sh.codes[r][e + q]).x;
+                            const float p = __fmul_rn(d, sc);
+                            acc[q] = SUM ? __fadd_rn(acc[q], p) : p;
+                        }
+                    }
+                }
+                for (int q = 0; q < 4; ++q) {
+                    if (e + q < n) {
+                        if (OUT_F32) out_f32[e + q] = acc[q];
+                        if (OUT_BF16) out_bf16[e + q] = (uint16_t)(pack_bf16x2(acc[q], 0.0f) & 0xFFFFu);
+                    }
                 }
             }
         }
-        store16<OUT_BF16, OUT_F32>(acc, e0, n, out_bf16, out_f32);
+        // every thread is done with stage s; refill it with this CTA's tile
+        // kRedStages steps ahead
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0) {
+            const size_t tn = t + (size_t)kRedStages * gridDim.x;
+            if (tn < nstaged) {
+                fence_proxy_async_smem();
+                issue(tn, s);
+            }
+        }
+    }
+    if (failed && tid == 0) {
+        // report, and let the copies still in flight land before the CTA's
+        // shared memory is released
+        raise_error(kErrCopyTimeout);
+        for (int j = it; j < it + kRedStages; ++j) {
+            const size_t tj = blockIdx.x + (size_t)j * gridDim.x;
+            if (tj < nstaged) mbar_wait(&full[j % kRedStages], (uint32_t)(j / kRedStages) & 1u);
+        }
     }
 }
 
@@ -131,13 +228,35 @@ sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, size_t slot, uint1
     }
 }
 
+template <int FMT, bool B, bool F, bool SUM, int KMAX>
+static fp8q_status_t launch_reduce_k(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
+    auto kernel = dequant_reduce_kernel<FMT, B, F, SUM, KMAX>;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [&] {
+        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)red_smem_bytes(KMAX));
+    });
+    if (attr_err != cudaSuccess) return cuda_status(attr_err);
+    static int resident[KMAX + 1] = {0};      // per k; benign race on first fill
+    const size_t smem = red_smem_bytes(k);
+    if (resident[k] == 0) resident[k] = resident_blocks(kernel, kRedThreads, smem);
+    const size_t tiles = (n + kRedTile - 1) / kRedTile;
+    const unsigned grid = grid_for(tiles, resident[k]);
+    kernel<<<grid, kRedThreads, smem, s>>>(sh, k, n, ob, of);
+    return launch_status();
+}
+
 template <int FMT, bool B, bool F, bool SUM>
 static fp8q_status_t launch_reduce_t(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
-    static int resident = resident_blocks(dequant_reduce_kernel<FMT, B, F, SUM>, kRedThreads);
-    const size_t units = (n + 15) / 16;
-    const unsigned grid = grid_for((units + kRedThreads - 1) / kRedThreads, resident);
-    dequant_reduce_kernel<FMT, B, F, SUM><<<grid, kRedThreads, 0, s>>>(sh, k, n, ob, of);
-    return launch_status();
+    if constexpr (!SUM) {
+        return launch_reduce_k<FMT, B, F, SUM, 1>(sh, k, n, ob, of, s);
+    } else {
+        if (k <= 2) return launch_reduce_k<FMT, B, F, SUM, 2>(sh, k, n, ob, of, s);
+        if (k <= 4) return launch_reduce_k<FMT, B, F, SUM, 4>(sh, k, n, ob, of, s);
+        if (k <= 8) return launch_reduce_k<FMT, B, F, SUM, 8>(sh, k, n, ob, of, s);
+        return launch_reduce_k<FMT, B, F, SUM, 16>(sh, k, n, ob, of, s);
+    }
 }
 
 template <int FMT, bool SUM>
@@ -185,6 +304,10 @@ static fp8q_status_t check_shards(const uint8_t* const* codes, const float* cons
     return FP8Q_OK;
 }
 
+}  // namespace fp8q
+
+namespace fp8q {
+unsigned unit_errors_reduce(bool clear) { return read_unit_errors(clear); }
 }  // namespace fp8q
 
 using namespace fp8q;

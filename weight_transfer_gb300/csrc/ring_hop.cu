@@ -8,51 +8,133 @@
 // the next hop, in one pass: the sums stay in registers while the block amax
 // is reduced, nothing is re-read from HBM.
 //
-// Work split: 8 lanes own one 128-element block; lane j holds elements
-// [8j, 8j+8) and [64+8j, 64+8j+8) (two 16-byte loads of the local partial,
-// two 8-byte loads of codes), so every load instruction of a warp reads whole
-// 128-byte (bf16) or 64-byte (codes) half-blocks.  The amax is a 3-step
-// xor-shuffle among the 8 lanes; a warp covers 4 blocks per step.  The
+// Work split: a persistent CTA of 256 threads walks tiles of 32 blocks
+// (4096 elements).  Thread 0 keeps up to kHopStages tiles in flight; a tile
+// is three bulk copies into one shared-memory stage (4096 incoming codes,
+// their 32 scales, 8 KB of the local bf16 partial) armed on the stage's
+// mbarrier.  Once it has landed, 8 lanes own one block: lane j takes
+// elements [8j, 8j+8) and [64+8j, 64+8j+8) (conflict-free shared-memory
+// reads), the amax is a 3-step xor-shuffle among the 8 lanes, and the
 // quotients y / s use the per-block reciprocal with two Markstein
-// corrections (exact for binary32 dividends, see block_quotients).
+// corrections (exact for binary32 dividends, see block_quotients).  The sums
+// stay in registers from the add to the requantization.  The ragged last
+// tile is read straight from global memory.
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
 namespace fp8q {
 
 constexpr int kHopThreads = 256;
+constexpr int kHopTileBlocks = 32;
+constexpr int kHopTile = kHopTileBlocks * 128;            // elements
+constexpr int kHopCodesBytes = kHopTile;
+constexpr int kHopScaleBytes = 4 * kHopTileBlocks;
+constexpr int kHopLocalBytes = 2 * kHopTile;
+constexpr int kHopStageBytes = kHopCodesBytes + kHopScaleBytes + kHopLocalBytes;
+constexpr int kHopStages = 3;
+constexpr size_t kHopSmem = (size_t)kHopStages * kHopStageBytes + 8 * kHopStages;
 
-template <int FMT, bool OUT_BF16>
+// Up to kHopMaxGroup independent hops in one launch (all ranks' hops of one
+// step of a ring simulated on one GPU).  Hop h owns the global tiles
+// [tile_start[h], tile_start[h + 1]).
+constexpr int kHopMaxGroup = FP8Q_MAX_HOP_GROUP;
+
+struct HopGroup {
+    const uint8_t* in_codes[kHopMaxGroup];
+    const float* in_scales[kHopMaxGroup];
+    const uint16_t* local[kHopMaxGroup];
+    uint8_t* out_codes[kHopMaxGroup];
+    float* out_scales[kHopMaxGroup];
+    uint16_t* out_bf16[kHopMaxGroup];          // may be null per hop
+    size_t n[kHopMaxGroup];
+    int64_t tile_start[kHopMaxGroup + 1];
+    int count;
+};
+
+template <int FMT>
 __global__ void __launch_bounds__(kHopThreads)
-ring_hop_kernel(const uint8_t* __restrict__ in_codes, const float* __restrict__ in_scales,
-                const uint16_t* local, size_t n, uint8_t* __restrict__ out_codes,
-                float* __restrict__ out_scales, uint16_t* out_bf16) {
-    const size_t nb = (n + 127) >> 7;
-    const size_t nfull = n >> 7;
-    const unsigned lane = threadIdx.x & 31u;
-    const unsigned j = lane & 7u;
-    const unsigned sub = lane >> 3;
-    const size_t warp = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const size_t nwarps = ((size_t)gridDim.x * blockDim.x) >> 5;
-    for (size_t base = warp; 4 * base < nb; base += nwarps) {    // warp-uniform bound
-        const size_t b = 4 * base + sub;
-        const size_t e0 = (b << 7) + 8 * j;
-        const long long avail = (long long)n - (long long)e0;      // valid elements from e0
-        uint2 ca = make_uint2(0u, 0u), cb = ca;
-        uint4 la = make_uint4(0u, 0u, 0u, 0u), lb = la;
-        float s_in = 0.0f;
-        if (b < nfull) {
-            ca = ld_stream8(in_codes + e0);
-            cb = ld_stream8(in_codes + e0 + 64);
-            la = ld_once(local + e0);
-            lb = ld_once(local + e0 + 64);
-        } else if (b < nb) {
-            ca = ld_u8x8_tail(in_codes + e0, avail);
-            cb = ld_u8x8_tail(in_codes + e0 + 64, avail - 64);
-            la = ld_bf16x8_tail(local + e0, avail);
-            lb = ld_bf16x8_tail(local + e0 + 64, avail - 64);
+ring_hop_kernel(const __grid_constant__ HopGroup g) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kHopStages * kHopStageBytes);
+    const int64_t total_tiles = g.tile_start[g.count];
+    const unsigned tid = threadIdx.x;
+    const unsigned lane = tid & 31u, warp = tid >> 5;
+    const unsigned j = lane & 7u, sub = lane >> 3;
+    const unsigned bl = warp * 4 + sub;                    // block inside the tile
+
+    auto hop_of = [&](int64_t t) {                         // CTA-uniform
+        int h = 0;
+        while (h + 1 < g.count && t >= g.tile_start[h + 1]) ++h;
+        return h;
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kHopStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // a tile is staged through shared memory when it lies entirely inside its hop's arrays
+    auto staged_tile = [&](int64_t t, int h) { return (size_t)(t - g.tile_start[h] + 1) * kHopTile <= g.n[h]; };
+    auto issue = [&](int64_t t, int h, int s) {   // thread 0 only
+        const size_t lt = (size_t)(t - g.tile_start[h]);
+        uint8_t* st = smem + (size_t)s * kHopStageBytes;
+        mbar_arrive_expect_tx(&full[s], kHopStageBytes);
+        bulk_g2s(st, g.in_codes[h] + lt * kHopTile, kHopCodesBytes, &full[s]);
+        bulk_g2s(st + kHopCodesBytes, g.in_scales[h] + lt * kHopTileBlocks, kHopScaleBytes, &full[s]);
+        bulk_g2s(st + kHopCodesBytes + kHopScaleBytes, g.local[h] + lt * kHopTile, kHopLocalBytes, &full[s]);
+    };
+    // A hop's ragged last tile is not staged and can sit between staged tiles,
+    // so each stage's barrier parity is tracked explicitly: bit s of `parity`
+    // is the phase to wait for on stage s, flipped each time a staged tile of
+    // that stage has been consumed.  `pending` (thread 0) marks stages with a
+    // copy issued and not yet consumed.
+    uint32_t parity = 0;
+    uint32_t pending = 0;
+    if (tid == 0)
+        for (int s = 0; s < kHopStages; ++s) {
+            const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+            if (t < total_tiles) {
+                const int h = hop_of(t);
+                if (staged_tile(t, h)) {
+                    issue(t, h, s);
+                    pending |= 1u << s;
+                }
+            }
         }
-        if (b < nb) s_in = ld_stream_f32(in_scales + b);
+
+    int it = 0;
+    bool failed = false;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const int s = it % kHopStages;
+        const int h = hop_of(t);
+        const size_t n = g.n[h];
+        const bool staged = staged_tile(t, h);
+        const bool ok = staged ? mbar_wait(&full[s], (parity >> s) & 1u) : true;
+        if (staged && ok) {
+            parity ^= 1u << s;
+            pending &= ~(1u << s);
+        }
+        const uint8_t* st = smem + (size_t)s * kHopStageBytes;
+        const size_t nb = (n + 127) >> 7;
+        const size_t b = (size_t)(t - g.tile_start[h]) * kHopTileBlocks + bl;
+        const size_t e0 = (b << 7) + 8 * j;
+        const long long avail = (long long)n - (long long)e0;     // valid elements from e0
+        uint2 ca, cb;
+        uint4 la, lb;
+        float s_in;
+        if (staged) {
+            ca = *reinterpret_cast<const uint2*>(st + bl * 128 + j * 8);
+            cb = *reinterpret_cast<const uint2*>(st + bl * 128 + 64 + j * 8);
+            s_in = *reinterpret_cast<const float*>(st + kHopCodesBytes + bl * 4);
+            const uint8_t* sl = st + kHopCodesBytes + kHopScaleBytes;
+            la = *reinterpret_cast<const uint4*>(sl + bl * 256 + j * 16);
+            lb = *reinterpret_cast<const uint4*>(sl + bl * 256 + 128 + j * 16);
+        } else {
+            ca = ld_u8x8_tail(g.in_codes[h] + e0, avail);
+            cb = ld_u8x8_tail(g.in_codes[h] + e0 + 64, avail - 64);
+            la = ld_bf16x8_tail(g.local[h] + e0, avail);
+            lb = ld_bf16x8_tail(g.local[h] + e0 + 64, avail - 64);
+            s_in = b < nb ? g.in_scales[h][b] : 0.0f;
+        }
 
         float d[16], lf[16], y[16];
         decode_fp8x4<FMT>(ca.x, d);
@@ -70,27 +152,30 @@ ring_hop_kernel(const uint8_t* __restrict__ in_codes, const float* __restrict__ 
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        const float s = block_scale<FMT>(a);
+        const float sc = block_scale<FMT>(a);
         float q[16];
-        block_quotients<2, 16>(y, s, q);
+        block_quotients<2, 16>(y, sc, q);
         uint32_t wa[2] = {cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])};
         uint32_t wb[2] = {cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]), cvt_fp8x4<FMT>(q[12], q[13], q[14], q[15])};
-        if (b < nfull) {
+        uint8_t* out_codes = g.out_codes[h];
+        uint16_t* out_bf16 = g.out_bf16[h];
+        if (staged) {
             st_stream(out_codes + e0, make_uint2(wa[0], wa[1]));
             st_stream(out_codes + e0 + 64, make_uint2(wb[0], wb[1]));
+            if (j == 0) g.out_scales[h][b] = sc;
         } else if (b < nb) {
             st_u8_tail(out_codes + e0, wa, 2, avail);
             st_u8_tail(out_codes + e0 + 64, wb, 2, avail - 64);
+            if (j == 0) g.out_scales[h][b] = sc;
         }
-        if (b < nb && j == 0) out_scales[b] = s;
-        if (OUT_BF16) {
+        if (out_bf16 != nullptr) {
             uint32_t ha[4], hb[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 ha[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
                 hb[i] = pack_bf16x2(y[8 + 2 * i], y[8 + 2 * i + 1]);
             }
-            if (b < nfull) {
+            if (staged) {
                 st_stream(out_bf16 + e0, make_uint4(ha[0], ha[1], ha[2], ha[3]));
                 st_stream(out_bf16 + e0 + 64, make_uint4(hb[0], hb[1], hb[2], hb[3]));
             } else if (b < nb) {
@@ -98,19 +183,121 @@ ring_hop_kernel(const uint8_t* __restrict__ in_codes, const float* __restrict__ 
                 st_u16_tail(out_bf16 + e0 + 64, hb, 4, avail - 64);
             }
         }
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0) {
+            const int64_t tn = t + (int64_t)kHopStages * gridDim.x;     // next tile of stage s
+            if (tn < total_tiles) {
+                const int hn = hop_of(tn);
+                if (staged_tile(tn, hn)) {
+                    fence_proxy_async_smem();
+                    issue(tn, hn, s);
+                    pending |= 1u << s;
+                }
+            }
+        }
+    }
+    if (failed && tid == 0) {
+        // report, and let the copies still in flight land before the CTA's
+        // shared memory is released
+        raise_error(kErrCopyTimeout);
+        for (int s = 0; s < kHopStages; ++s)
+            if (pending & (1u << s)) mbar_wait(&full[s], (parity >> s) & 1u);
     }
 }
 
-template <int FMT, bool B>
-static fp8q_status_t launch_hop_t(const uint8_t* ic, const float* is, const uint16_t* loc, size_t n, uint8_t* oc,
-                                  float* os, uint16_t* ob, cudaStream_t s) {
-    static int resident = resident_blocks(ring_hop_kernel<FMT, B>, kHopThreads);
-    const size_t blocks_per_cta = (kHopThreads / 32) * 4;
-    const unsigned grid = grid_for(((n + 127) / 128 + blocks_per_cta - 1) / blocks_per_cta, resident);
-    ring_hop_kernel<FMT, B><<<grid, kHopThreads, 0, s>>>(ic, is, loc, n, oc, os, ob);
+// Host checks of one hop (as documented for fp8q_ring_hop).
+static fp8q_status_t check_hop(const fp8q_hop_t& hp) {
+    if (hp.n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
+    if (hp.n == 0) return FP8Q_OK;
+    if (!hp.in_codes || !hp.in_scales || !hp.local_bf16 || !hp.out_codes || !hp.out_scales) return FP8Q_ERR_NULL;
+    if (!aligned16(hp.in_codes) || !aligned16(hp.in_scales) || !aligned16(hp.local_bf16) ||
+        !aligned16(hp.out_codes) || !aligned16(hp.out_scales) || (hp.out_bf16 && !aligned16(hp.out_bf16)))
+        return FP8Q_ERR_ALIGN;
+    return FP8Q_OK;
+}
+
+// Byte ranges of a hop: reads 0..2, writes 3..5.
+static void hop_ranges(const fp8q_hop_t& hp, const void* p[6], size_t sz[6]) {
+    const size_t n = hp.n, nb = fp8q_num_scales(n);
+    p[0] = hp.in_codes;  sz[0] = n;
+    p[1] = hp.in_scales; sz[1] = 4 * nb;
+    p[2] = hp.local_bf16; sz[2] = 2 * n;
+    p[3] = hp.out_codes; sz[3] = n;
+    p[4] = hp.out_scales; sz[4] = 4 * nb;
+    p[5] = hp.out_bf16;  sz[5] = hp.out_bf16 ? 2 * n : 0;
+}
+
+static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, cudaStream_t stream) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
+    if (!hops) return FP8Q_ERR_NULL;
+    if (count < 1 || count > kHopMaxGroup) return FP8Q_ERR_SIZE;
+    for (int i = 0; i < count; ++i) {
+        const fp8q_status_t st = check_hop(hops[i]);
+        if (st != FP8Q_OK) return st;
+    }
+    // no output may overlap another output or any input of the group; the one
+    // exception is a hop's bf16 output written in place over its own local partial
+    for (int i = 0; i < count; ++i) {
+        if (hops[i].n == 0) continue;
+        const void* pi[6];
+        size_t si[6];
+        hop_ranges(hops[i], pi, si);
+        for (int j = 0; j < count; ++j) {
+            if (hops[j].n == 0) continue;
+            const void* pj[6];
+            size_t sj[6];
+            hop_ranges(hops[j], pj, sj);
+            for (int a = 3; a < 6; ++a)
+                for (int b = 0; b < 6; ++b) {
+                    if (i == j && a == b) continue;
+                    if (i == j && a == 5 && b == 2 && pi[5] == pj[2]) continue;
+                    if (overlaps(pi[a], si[a], pj[b], sj[b])) return FP8Q_ERR_ALIAS;
+                }
+        }
+    }
+    HopGroup g;
+    int used = 0;
+    int64_t start = 0;
+    for (int i = 0; i < count; ++i) {
+        const fp8q_hop_t& hp = hops[i];
+        if (hp.n == 0) continue;
+        g.in_codes[used] = hp.in_codes;
+        g.in_scales[used] = hp.in_scales;
+        g.local[used] = static_cast<const uint16_t*>(hp.local_bf16);
+        g.out_codes[used] = hp.out_codes;
+        g.out_scales[used] = hp.out_scales;
+        g.out_bf16[used] = static_cast<uint16_t*>(hp.out_bf16);
+        g.n[used] = hp.n;
+        g.tile_start[used] = start;
+        start += (int64_t)((hp.n + kHopTile - 1) / kHopTile);
+        ++used;
+    }
+    if (used == 0) return FP8Q_OK;
+    g.tile_start[used] = start;
+    g.count = used;
+    const bool e4 = fmt == FP8Q_E4M3;
+    static const cudaError_t attr4 =
+        cudaFuncSetAttribute(ring_hop_kernel<kE4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHopSmem);
+    static const cudaError_t attr5 =
+        cudaFuncSetAttribute(ring_hop_kernel<kE5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHopSmem);
+    if ((e4 ? attr4 : attr5) != cudaSuccess) return cuda_status(e4 ? attr4 : attr5);
+    static int resident4 = resident_blocks(ring_hop_kernel<kE4M3>, kHopThreads, kHopSmem);
+    static int resident5 = resident_blocks(ring_hop_kernel<kE5M2>, kHopThreads, kHopSmem);
+    const unsigned grid = grid_for((size_t)start, e4 ? resident4 : resident5);
+    if (e4)
+        ring_hop_kernel<kE4M3><<<grid, kHopThreads, kHopSmem, stream>>>(g);
+    else
+        ring_hop_kernel<kE5M2><<<grid, kHopThreads, kHopSmem, stream>>>(g);
     return launch_status();
 }
 
+}  // namespace fp8q
+
+namespace fp8q {
+unsigned unit_errors_ring_hop(bool clear) { return read_unit_errors(clear); }
 }  // namespace fp8q
 
 using namespace fp8q;
@@ -118,32 +305,11 @@ using namespace fp8q;
 extern "C" fp8q_status_t fp8q_ring_hop(const uint8_t* in_codes, const float* in_scales, const void* local_bf16,
                                        size_t n, fp8q_format_t fmt, uint8_t* out_codes, float* out_scales,
                                        void* out_bf16, fp8q_stream_t stream) {
-    if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
-    if (n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
-    if (n == 0) return FP8Q_OK;
-    if (!in_codes || !in_scales || !local_bf16 || !out_codes || !out_scales) return FP8Q_ERR_NULL;
-    if (!aligned16(in_codes) || !aligned16(in_scales) || !aligned16(local_bf16) || !aligned16(out_codes) ||
-        !aligned16(out_scales) || (out_bf16 && !aligned16(out_bf16)))
-        return FP8Q_ERR_ALIGN;
-    const size_t nb = fp8q_num_scales(n);
-    const void* ins[3] = {in_codes, in_scales, local_bf16};
-    const size_t in_sz[3] = {n, 4 * nb, 2 * n};
-    void* outs[3] = {out_codes, out_scales, out_bf16};
-    const size_t out_sz[3] = {n, 4 * nb, 2 * n};
-    for (int o = 0; o < 3; ++o) {
-        for (int i = 0; i < 3; ++i) {
-            if (o == 2 && i == 2 && outs[2] == ins[2]) continue;   // in-place update of the local partial
-            if (overlaps(outs[o], out_sz[o], ins[i], in_sz[i])) return FP8Q_ERR_ALIAS;
-        }
-        for (int p = o + 1; p < 3; ++p)
-            if (overlaps(outs[o], out_sz[o], outs[p], out_sz[p])) return FP8Q_ERR_ALIAS;
-    }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const uint16_t* loc = static_cast<const uint16_t*>(local_bf16);
-    uint16_t* ob = static_cast<uint16_t*>(out_bf16);
-    if (fmt == FP8Q_E4M3)
-        return ob ? launch_hop_t<kE4M3, true>(in_codes, in_scales, loc, n, out_codes, out_scales, ob, s)
-                  : launch_hop_t<kE4M3, false>(in_codes, in_scales, loc, n, out_codes, out_scales, ob, s);
-    return ob ? launch_hop_t<kE5M2, true>(in_codes, in_scales, loc, n, out_codes, out_scales, ob, s)
-              : launch_hop_t<kE5M2, false>(in_codes, in_scales, loc, n, out_codes, out_scales, ob, s);
+    const fp8q_hop_t hp = {in_codes, in_scales, local_bf16, n, out_codes, out_scales, out_bf16};
+    return launch_hops(&hp, 1, fmt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8q_status_t fp8q_ring_hop_group(const fp8q_hop_t* hops, int count, fp8q_format_t fmt,
+                                             fp8q_stream_t stream) {
+    return launch_hops(hops, count, fmt, reinterpret_cast<cudaStream_t>(stream));
 }
