@@ -156,6 +156,23 @@ fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, void* const* 
                                       fp8q_format_t fmt, void* workspace, size_t workspace_bytes,
                                       uint64_t* wire_bytes, fp8q_stream_t stream);
 
+/* ------------------------------------------------------------ variants ----
+ * fp8q_quantize_tensorwise: one scale for the whole tensor (the tensorwise
+ *   recipe of TorchAO's Float8Linear that [P2] uses for its FP8 GEMMs):
+ *   amax = max |x_i|, s = RN(amax / Fmax), c_i = satfinite RNE_fp8(RN(x_i/s)),
+ *   i.e. (a) with one block of n elements.  scale_amax: 2 device floats,
+ *   [0] = s and [1] = amax on return (the call clears [1] first, with a
+ *   cudaMemsetAsync on `stream`).
+ * fp8q_ring_hop_bf16_requant: fp8q_ring_hop, but the block is requantized
+ *   from RNE_bf16(y) -- the bf16 partial a receiver keeps -- instead of the
+ *   fp32 sum y (the other reading of "adds it to the local bf16 partial and
+ *   requantizes").  Same arguments and rules as fp8q_ring_hop. */
+fp8q_status_t fp8q_quantize_tensorwise(const void* x_bf16, size_t n, fp8q_format_t fmt, uint8_t* codes,
+                                       float* scale_amax, fp8q_stream_t stream);
+fp8q_status_t fp8q_ring_hop_bf16_requant(const uint8_t* in_codes, const float* in_scales, const void* local_bf16,
+                                         size_t n, fp8q_format_t fmt, uint8_t* out_codes, float* out_scales,
+                                         void* out_bf16, fp8q_stream_t stream);
+
 /* ---------------------------------------------------------------- (d) ----
  * BF16 -> MXFP8 weight prequantization ([P3] Summary, self-review).
  * w is [batch, m, k] row-major ([out, in] weights, batch = experts); every
@@ -215,6 +232,47 @@ fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, int64_t bat
                                      uint8_t* scales_rowmajor, fp8q_stream_t stream);
 fp8q_status_t fp8q_count_mismatches(const void* a, const void* b, size_t nbytes, unsigned long long* count,
                                     fp8q_stream_t stream);
+
+/* ----------------------------------------------------- transfer packing ----
+ * [P3] inline review: weights and their scales travel as separate entries
+ * through size-capped transfer batches, a weight (~32x its scale) usually
+ * closes a batch and its scale opens the next, and the receiver's per-batch
+ * check then fails; oversized parameters travel alone.  The fix it names is
+ * packing weight and scale atomically.
+ *
+ * fp8q_pack_plan (host only, no GPU): items[i] is the byte size of weight
+ *   i's codes and of its scales.  Every pair goes whole into one batch:
+ *   codes at slots[i].codes_offset, scales at slots[i].scales_offset of
+ *   batch slots[i].batch (16-byte aligned offsets).  Pairs are taken in
+ *   order; a pair that does not fit in the current batch (cap_bytes) opens
+ *   the next one, and a pair larger than the cap gets a batch of its own.
+ *   batch_bytes (room for `count` entries) receives each batch's size,
+ *   *num_batches their number.
+ * fp8q_copy_segments: one launch copying up to FP8Q_MAX_COPY_SEGMENTS
+ *   device byte ranges (the gather of a plan's pairs into a transfer
+ *   buffer, or the scatter out of it on the receiver).  src and dst 16-byte
+ *   aligned, any byte count; destinations must not overlap each other or any
+ *   source (FP8Q_ERR_ALIAS). */
+typedef struct {
+    uint64_t codes_bytes, scales_bytes;
+} fp8q_pack_item_t;
+
+typedef struct {
+    int32_t batch;
+    uint64_t codes_offset, scales_offset;
+} fp8q_pack_slot_t;
+
+typedef struct {
+    const void* src;
+    void* dst;
+    uint64_t bytes;
+} fp8q_copy_t;
+
+#define FP8Q_MAX_COPY_SEGMENTS 96
+
+fp8q_status_t fp8q_pack_plan(const fp8q_pack_item_t* items, int count, uint64_t cap_bytes, fp8q_pack_slot_t* slots,
+                             uint64_t* batch_bytes, int* num_batches);
+fp8q_status_t fp8q_copy_segments(const fp8q_copy_t* segs, int count, fp8q_stream_t stream);
 
 /* ------------------------------------------------------------- helpers ---- */
 

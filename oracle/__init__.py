@@ -17,6 +17,9 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*``):
   dequant_reduce, ring_hop           pinned (exact rational sums within the
                                      fp32 recursive-summation bound)
   mxfp8 block codes and E8M0         pinned (hand examples, invariants)
+  quantize_tensorwise                pinned (one block: equals the blockwise
+                                     quantizer; power-of-two scales vs torch)
+  ring_hop_bf16_requant              pinned (equals quantize of the bf16 sum)
   mxfp8 dequantize / unswizzle       pinned (torch float8 decode times a power
                                      of two; round trip; the hand swizzle table)
   scale swizzle                      formula pinned by a hand table and a
@@ -102,6 +105,8 @@ def lib() -> ctypes.CDLL:
         L.orc_mxfp8_dequantize.argtypes = [_u8p, _u8p, _i64, _i64, _i64, _u16p]
         L.orc_count_mismatches.argtypes = [_u8p, _u8p, _sz]
         L.orc_count_mismatches.restype = ctypes.c_uint64
+        L.orc_quantize_tensorwise.argtypes = [_u16p, _sz, ctypes.c_int, _u8p, _f32p, _f32p]
+        L.orc_ring_hop_bf16_requant.argtypes = [_u8p, _f32p, _u16p, _sz, ctypes.c_int, _u8p, _f32p, _u16p]
         _lib = L
     return _lib
 
@@ -275,3 +280,27 @@ def count_mismatches(a, b) -> int:
     b = np.ascontiguousarray(b, dtype=np.uint8).ravel()
     assert a.size == b.size
     return int(lib().orc_count_mismatches(_p(a, _u8p), _p(b, _u8p), a.size))
+
+
+def quantize_tensorwise(x, fmt: int):
+    """bf16[n] -> (codes u8[n], scale, amax) with one scale for the tensor."""
+    x = _bf16_bits(x)
+    codes = np.empty(x.size, np.uint8)
+    sc = np.zeros(1, np.float32)
+    am = np.zeros(1, np.float32)
+    lib().orc_quantize_tensorwise(_p(x, _u16p), x.size, fmt, _p(codes, _u8p), _p(sc, _f32p), _p(am, _f32p))
+    return codes, sc[0], am[0]
+
+
+def ring_hop_bf16_requant(in_codes, in_scales, local, fmt: int):
+    """ring_hop, but requantizing RNE_bf16(y) instead of y."""
+    in_codes = np.ascontiguousarray(in_codes, dtype=np.uint8)
+    in_scales = np.ascontiguousarray(in_scales, dtype=np.float32)
+    local = _bf16_bits(local)
+    n = in_codes.size
+    oc = np.empty(n, np.uint8)
+    os_ = np.empty(num_blocks(n), np.float32)
+    ob = np.empty(n, np.uint16)
+    lib().orc_ring_hop_bf16_requant(_p(in_codes, _u8p), _p(in_scales, _f32p), _p(local, _u16p), n, fmt,
+                                    _p(oc, _u8p), _p(os_, _f32p), _p(ob, _u16p))
+    return oc, os_, ob

@@ -382,4 +382,53 @@ uint64_t orc_count_mismatches(const uint8_t* a, const uint8_t* b, size_t n) {
     return c;
 }
 
+// -------------------------------------------------- tensorwise scaling ----
+// "How to Speed Up VLA Training Step by Step", FP8 paragraph: TorchAO's
+// tensorwise recipe computes one amax and one scale for the whole tensor.
+// Same arithmetic as (a) with a single block spanning all n elements:
+//   amax = max |x_i|, s = RN(amax / Fmax), c_i = satfinite RNE_fp8(RN(x_i / s)).
+// Writes s and amax.
+void orc_quantize_tensorwise(const uint16_t* x, size_t n, int fmt, uint8_t* codes, float* scale, float* amax_out) {
+    const Fmt& F = fmt_of(fmt);
+    float amax = 0.0f;
+    for (size_t i = 0; i < n; ++i) {
+        float a = std::fabs(bf16_to_f32(x[i]));
+        if (a > amax) amax = a;
+    }
+    float s = amax / F.max_value;
+    for (size_t i = 0; i < n; ++i) {
+        float xi = bf16_to_f32(x[i]);
+        codes[i] = encode_bits(F, s == 0.0f ? xi : xi / s);
+    }
+    *scale = s;
+    *amax_out = amax;
+}
+
+// The ring hop variant that requantizes RNE_bf16(y) (the bf16 partial a
+// receiver would keep) instead of the fp32 sum y: reading O9's alternative.
+void orc_ring_hop_bf16_requant(const uint8_t* in_codes, const float* in_scales, const uint16_t* local, size_t n,
+                               int fmt, uint8_t* out_codes, float* out_scales, uint16_t* out_bf16) {
+    const Fmt& F = fmt_of(fmt);
+    size_t nb = (n + 127) / 128;
+    float y[128];
+    for (size_t b = 0; b < nb; ++b) {
+        size_t lo = b * 128, hi = lo + 128 < n ? lo + 128 : n;
+        float amax = 0.0f;
+        for (size_t i = lo; i < hi; ++i) {
+            float d = decode_f(F, in_codes[i]) * in_scales[b];
+            float yi = bf16_to_f32(f32_to_bf16(d + bf16_to_f32(local[i])));
+            y[i - lo] = yi;
+            float a = std::fabs(yi);
+            if (a > amax) amax = a;
+        }
+        float s = amax / F.max_value;
+        out_scales[b] = s;
+        for (size_t i = lo; i < hi; ++i) {
+            float yi = y[i - lo];
+            out_codes[i] = encode_bits(F, s == 0.0f ? yi : yi / s);
+            if (out_bf16) out_bf16[i] = f32_to_bf16(yi);
+        }
+    }
+}
+
 }  // extern "C"

@@ -518,3 +518,40 @@ def test_count_mismatches(orc):
     b = a.copy()
     b[[3, 500, 999]] ^= 1
     assert orc.count_mismatches(a, a) == 0 and orc.count_mismatches(a, b) == 3
+
+
+# --------------------------------------------------------- NEXT variants --
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_tensorwise_equals_blockwise_on_one_block(orc, fmt):
+    # with n <= 128 the tensor is one block: both recipes must agree
+    for n in (1, 77, 128):
+        xb = bf16_bits((np.random.default_rng(n).standard_normal(n) * 3e-3).astype(np.float32))
+        c1, s1 = orc.quantize_blockwise(xb, fmt)
+        c2, s2, a2 = orc.quantize_tensorwise(xb, fmt)
+        assert np.array_equal(c1, c2) and s1[0] == s2
+        assert a2 == np.abs(bf16_val(xb)).max()
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_tensorwise_power_of_two_scale(orc, fmt):
+    # amax = Fmax * 2^-9 over many blocks -> s = 2^-9, codes are torch's
+    # conversion of x * 2^9
+    rng = np.random.default_rng(90 + fmt)
+    x = np.clip(rng.standard_normal(5000) * FMAX[fmt] * 2.0 ** -11, -FMAX[fmt] * 2.0 ** -9, FMAX[fmt] * 2.0 ** -9)
+    x[1234] = FMAX[fmt] * 2.0 ** -9
+    xb = bf16_bits(x.astype(np.float32))
+    codes, s, amax = orc.quantize_tensorwise(xb, fmt)
+    assert s == np.float32(2.0 ** -9) and amax == np.float32(FMAX[fmt] * 2.0 ** -9)
+    assert np.array_equal(codes, torch_fp8(fmt, bf16_val(xb) * np.float32(2.0 ** 9)))
+
+
+def test_ring_hop_bf16_requant_equals_quantize_of_bf16_sum(orc):
+    rng = np.random.default_rng(91)
+    n = 128 * 9 + 5
+    codes, scales = orc.quantize_blockwise(bf16_bits((rng.standard_normal(n) * 1e-3).astype(np.float32)), 0)
+    loc = bf16_bits((rng.standard_normal(n) * 1e-3).astype(np.float32))
+    oc, os_, ob = orc.ring_hop_bf16_requant(codes, scales, loc, 0)
+    _, _, ob32 = orc.ring_hop(codes, scales, loc, 0)
+    assert np.array_equal(ob, ob32)                      # same bf16 partial
+    qc, qs = orc.quantize_blockwise(ob, 0)               # requantized from it
+    assert np.array_equal(oc, qc) and np.array_equal(os_, qs)

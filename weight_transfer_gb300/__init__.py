@@ -64,6 +64,21 @@ class mxfp8_tensor_t(ctypes.Structure):
 
 MXFP8_MAX_GROUP = 16
 
+
+class fp8q_pack_item_t(ctypes.Structure):
+    _fields_ = [("codes_bytes", ctypes.c_uint64), ("scales_bytes", ctypes.c_uint64)]
+
+
+class fp8q_pack_slot_t(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("codes_offset", ctypes.c_uint64), ("scales_offset", ctypes.c_uint64)]
+
+
+class fp8q_copy_t(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_void_p), ("dst", ctypes.c_void_p), ("bytes", ctypes.c_uint64)]
+
+
+FP8Q_MAX_COPY_SEGMENTS = 96
+
 # name -> (argtypes, restype)
 _SIGNATURES = {
     "fp8q_quantize_blockwise": ([_vp, _sz, _int, _vp, _vp, _vp], _int),
@@ -74,6 +89,11 @@ _SIGNATURES = {
     "mxfp8_dequantize_swizzled": ([_vp, _vp, _i64, _i64, _i64, _vp, _vp], _int),
     "mxfp8_unswizzle_scales": ([_vp, _i64, _i64, _i64, _vp, _vp], _int),
     "fp8q_count_mismatches": ([_vp, _vp, _sz, _vp, _vp], _int),
+    "fp8q_quantize_tensorwise": ([_vp, _sz, _int, _vp, _vp, _vp], _int),
+    "fp8q_ring_hop_bf16_requant": ([_vp, _vp, _vp, _sz, _int, _vp, _vp, _vp, _vp], _int),
+    "fp8q_pack_plan": ([ctypes.POINTER(fp8q_pack_item_t), _int, ctypes.c_uint64, ctypes.POINTER(fp8q_pack_slot_t),
+                        ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_int)], _int),
+    "fp8q_copy_segments": ([ctypes.POINTER(fp8q_copy_t), _int, _vp], _int),
     "fp8q_ring_hop_group": ([ctypes.POINTER(fp8q_hop_t), _int, _int, _vp], _int),
     "fp8q_ring_allreduce_workspace_bytes": ([_int, _sz], _sz),
     "fp8q_ring_allreduce_sim": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _sz,
@@ -379,6 +399,63 @@ def fp8q_count_mismatches(a: torch.Tensor, b: torch.Tensor, count: Optional[torc
                                      _stream(stream))
     _check("fp8q_count_mismatches", st)
     return count
+
+
+def fp8q_quantize_tensorwise(x: torch.Tensor, fmt="e4m3", codes: Optional[torch.Tensor] = None,
+                             scale_amax: Optional[torch.Tensor] = None, stream=None):
+    """bf16 x -> (codes uint8 [n], float32 [2] device tensor holding (scale, amax))."""
+    n = x.numel()
+    if codes is None:
+        codes = torch.empty(n, dtype=torch.uint8, device=x.device)
+    if scale_amax is None:
+        scale_amax = torch.empty(4, dtype=torch.float32, device=x.device)
+    st = lib().fp8q_quantize_tensorwise(_dev(x, "x", torch.bfloat16), n, _fmt(fmt),
+                                        _dev(codes, "codes", torch.uint8, n),
+                                        _dev(scale_amax, "scale_amax", torch.float32, 2), _stream(stream))
+    _check("fp8q_quantize_tensorwise", st)
+    return codes, scale_amax[:2]
+
+
+def fp8q_ring_hop_bf16_requant(in_codes: torch.Tensor, in_scales: torch.Tensor, local: torch.Tensor, fmt="e4m3",
+                               want_bf16: bool = False, stream=None):
+    """fp8q_ring_hop that requantizes the bf16-rounded sum -> (codes, scales, bf16 or None)."""
+    n = local.numel()
+    dev = local.device
+    nb = fp8q_num_scales(n)
+    oc = torch.empty(n, dtype=torch.uint8, device=dev)
+    os_ = torch.empty(max(nb, 1), dtype=torch.float32, device=dev)
+    ob = torch.empty(n, dtype=torch.bfloat16, device=dev) if want_bf16 else None
+    st = lib().fp8q_ring_hop_bf16_requant(_dev(in_codes, "in_codes", torch.uint8, n),
+                                          _dev(in_scales, "in_scales", torch.float32, nb),
+                                          _dev(local, "local", torch.bfloat16), n, _fmt(fmt), _dev(oc, "out_codes"),
+                                          _dev(os_, "out_scales"), _dev(ob, "out_bf16"), _stream(stream))
+    _check("fp8q_ring_hop_bf16_requant", st)
+    return oc, os_, ob
+
+
+def fp8q_pack_plan(pairs: Sequence[tuple], cap_bytes: int):
+    """pairs: (codes_bytes, scales_bytes) per weight -> (list of
+    (batch, codes_offset, scales_offset), list of batch sizes)."""
+    n = len(pairs)
+    items = (fp8q_pack_item_t * max(n, 1))(*[fp8q_pack_item_t(int(c), int(s)) for c, s in pairs])
+    slots = (fp8q_pack_slot_t * max(n, 1))()
+    sizes = (ctypes.c_uint64 * max(n, 1))()
+    nb = _int(0)
+    _check("fp8q_pack_plan", lib().fp8q_pack_plan(items, n, cap_bytes, slots, sizes, ctypes.byref(nb)))
+    return [(slots[i].batch, slots[i].codes_offset, slots[i].scales_offset) for i in range(n)], \
+        [int(sizes[b]) for b in range(nb.value)]
+
+
+def fp8q_copy_segments(segments: Sequence[tuple], stream=None):
+    """segments: (src tensor, dst tensor view) pairs of equal byte size; one launch."""
+    n = len(segments)
+    arr = (fp8q_copy_t * max(n, 1))()
+    for i, (src, dst) in enumerate(segments):
+        nbytes = src.numel() * src.element_size()
+        if dst.numel() * dst.element_size() != nbytes:
+            raise ValueError(f"segment {i}: source and destination sizes differ")
+        arr[i] = fp8q_copy_t(_dev(src, f"segments[{i}].src"), _dev(dst, f"segments[{i}].dst"), nbytes)
+    _check("fp8q_copy_segments", lib().fp8q_copy_segments(arr, n, _stream(stream)))
 
 
 def fp8q_encode_f32(x: torch.Tensor, fmt="e4m3", codes: Optional[torch.Tensor] = None, stream=None):

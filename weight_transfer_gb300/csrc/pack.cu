@@ -1,0 +1,125 @@
+// Packing prequantized weights and their scales into size-capped transfer
+// buffers, each weight together with its scale.
+//
+// "perf: Reduce MXFP8 refit weight-transfer overheads", inline review: the
+// sender yields an E4M3 weight and then its *_scale_from_checkpoint as two
+// entries, every transport batches by size with no pairing constraint, and a
+// weight (about 32x its scale) usually closes a buffer so that its scale
+// opens the next one -- the receiver's per-batch presence check then fails
+// on a healthy stream; oversized parameters are shipped alone.  The review's
+// third fix is to pack weight and scale atomically.  Here:
+//   fp8q_pack_plan      (host) assigns every (codes, scales) pair to a batch
+//                       whole: a pair that does not fit in the current batch
+//                       opens the next one, a pair larger than the cap gets a
+//                       batch of its own; offsets are 16-byte aligned;
+//   fp8q_copy_segments  (device) one launch that moves many byte ranges
+//                       (the gather into a transfer buffer, or the scatter
+//                       out of it), split into 64 KiB pieces over a
+//                       persistent grid with 16-byte loads and stores.
+#include "fp8q_host.cuh"
+#include "fp8q_device.cuh"
+
+namespace fp8q {
+
+constexpr int kMaxSegments = FP8Q_MAX_COPY_SEGMENTS;
+constexpr uint64_t kPiece = 64 * 1024;      // bytes per CTA step
+
+struct SegmentTable {
+    const uint8_t* src[kMaxSegments];
+    uint8_t* dst[kMaxSegments];
+    uint64_t bytes[kMaxSegments];
+    uint64_t piece_start[kMaxSegments + 1];
+    int count;
+};
+
+__global__ void __launch_bounds__(256) copy_segments_kernel(const __grid_constant__ SegmentTable tab) {
+    const uint64_t pieces = tab.piece_start[tab.count];
+    for (uint64_t p = blockIdx.x; p < pieces; p += gridDim.x) {
+        int lo = 0, hi = tab.count - 1;                 // segment with piece_start <= p < next
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (tab.piece_start[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        const int s = lo;
+        const uint64_t off = (p - tab.piece_start[s]) * kPiece;
+        const uint64_t len = min(kPiece, tab.bytes[s] - off);
+        const uint8_t* src = tab.src[s] + off;
+        uint8_t* dst = tab.dst[s] + off;
+        const uint64_t n16 = len / 16;
+        for (uint64_t i = threadIdx.x; i < n16; i += blockDim.x)
+            st_stream(dst + 16 * i, ld_stream(src + 16 * i));
+        for (uint64_t i = 16 * n16 + threadIdx.x; i < len; i += blockDim.x) dst[i] = src[i];
+    }
+}
+
+inline uint64_t round16(uint64_t b) { return (b + 15) & ~(uint64_t)15; }
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" fp8q_status_t fp8q_pack_plan(const fp8q_pack_item_t* items, int count, uint64_t cap_bytes,
+                                        fp8q_pack_slot_t* slots, uint64_t* batch_bytes, int* num_batches) {
+    if (count < 0) return FP8Q_ERR_SIZE;
+    if (!num_batches) return FP8Q_ERR_NULL;
+    *num_batches = 0;
+    if (count == 0) return FP8Q_OK;
+    if (!items || !slots || !batch_bytes) return FP8Q_ERR_NULL;
+    if (cap_bytes < 16) return FP8Q_ERR_SIZE;
+    int batch = 0;
+    uint64_t fill = 0;
+    for (int i = 0; i < count; ++i) {
+        const uint64_t c = round16(items[i].codes_bytes), s = round16(items[i].scales_bytes);
+        const uint64_t pair = c + s;
+        if (fill > 0 && fill + pair > cap_bytes) {      // the pair does not fit: close the batch
+            batch_bytes[batch++] = fill;
+            fill = 0;
+        }
+        slots[i].batch = batch;
+        slots[i].codes_offset = fill;
+        slots[i].scales_offset = fill + c;
+        fill += pair;
+        if (fill >= cap_bytes) {                        // full, or an oversized pair alone
+            batch_bytes[batch++] = fill;
+            fill = 0;
+        }
+    }
+    if (fill > 0) batch_bytes[batch++] = fill;
+    *num_batches = batch;
+    return FP8Q_OK;
+}
+
+extern "C" fp8q_status_t fp8q_copy_segments(const fp8q_copy_t* segs, int count, fp8q_stream_t stream) {
+    if (count < 0 || count > kMaxSegments) return FP8Q_ERR_SIZE;
+    if (count == 0) return FP8Q_OK;
+    if (!segs) return FP8Q_ERR_NULL;
+    SegmentTable tab;
+    int used = 0;
+    uint64_t pieces = 0;
+    for (int i = 0; i < count; ++i) {
+        const fp8q_copy_t& c = segs[i];
+        if (c.bytes == 0) continue;
+        if (c.bytes > 16 * FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
+        if (!c.src || !c.dst) return FP8Q_ERR_NULL;
+        if (!aligned16(c.src) || !aligned16(c.dst)) return FP8Q_ERR_ALIGN;
+        if (overlaps(c.dst, c.bytes, c.src, c.bytes)) return FP8Q_ERR_ALIAS;
+        for (int j = 0; j < i; ++j)                     // destinations are disjoint, and no
+            if (segs[j].bytes &&                        // destination is another segment's source
+                (overlaps(c.dst, c.bytes, segs[j].dst, segs[j].bytes) ||
+                 overlaps(c.dst, c.bytes, segs[j].src, segs[j].bytes) ||
+                 overlaps(segs[j].dst, segs[j].bytes, c.src, c.bytes)))
+                return FP8Q_ERR_ALIAS;
+        tab.src[used] = static_cast<const uint8_t*>(c.src);
+        tab.dst[used] = static_cast<uint8_t*>(c.dst);
+        tab.bytes[used] = c.bytes;
+        tab.piece_start[used] = pieces;
+        pieces += (c.bytes + kPiece - 1) / kPiece;
+        ++used;
+    }
+    if (used == 0) return FP8Q_OK;
+    tab.piece_start[used] = pieces;
+    tab.count = used;
+    static int resident = resident_blocks(copy_segments_kernel, 256);
+    copy_segments_kernel<<<grid_for((size_t)pieces, resident), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(tab);
+    return launch_status();
+}

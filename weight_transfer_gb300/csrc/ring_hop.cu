@@ -51,7 +51,9 @@ struct HopGroup {
     int count;
 };
 
-template <int FMT>
+// REQ_BF16: requantize RNE_bf16(y), the bf16 partial a receiver keeps,
+// instead of the fp32 sum y (the alternative reading of the hop).
+template <int FMT, bool REQ_BF16>
 __global__ void __launch_bounds__(kHopThreads)
 ring_hop_kernel(const __grid_constant__ HopGroup g) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -147,6 +149,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             y[i] = __fadd_rn(__fmul_rn(d[i], s_in), lf[i]);
+            if (REQ_BF16) y[i] = bf16_lo(pack_bf16x2(y[i], 0.0f));
             a = fmaxf(a, fabsf(y[i]));
         }
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
@@ -230,7 +233,18 @@ static void hop_ranges(const fp8q_hop_t& hp, const void* p[6], size_t sz[6]) {
     p[5] = hp.out_bf16;  sz[5] = hp.out_bf16 ? 2 * n : 0;
 }
 
-static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, cudaStream_t stream) {
+template <int FMT, bool REQ>
+static fp8q_status_t launch_hop_kernel(const HopGroup& g, size_t tiles, cudaStream_t stream) {
+    static const cudaError_t attr = cudaFuncSetAttribute(ring_hop_kernel<FMT, REQ>,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHopSmem);
+    if (attr != cudaSuccess) return cuda_status(attr);
+    static int resident = resident_blocks(ring_hop_kernel<FMT, REQ>, kHopThreads, kHopSmem);
+    ring_hop_kernel<FMT, REQ><<<grid_for(tiles, resident), kHopThreads, kHopSmem, stream>>>(g);
+    return launch_status();
+}
+
+static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, cudaStream_t stream,
+                                 bool requant_bf16 = false) {
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
     if (!hops) return FP8Q_ERR_NULL;
     if (count < 1 || count > kHopMaxGroup) return FP8Q_ERR_SIZE;
@@ -278,20 +292,12 @@ static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_
     if (used == 0) return FP8Q_OK;
     g.tile_start[used] = start;
     g.count = used;
-    const bool e4 = fmt == FP8Q_E4M3;
-    static const cudaError_t attr4 =
-        cudaFuncSetAttribute(ring_hop_kernel<kE4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHopSmem);
-    static const cudaError_t attr5 =
-        cudaFuncSetAttribute(ring_hop_kernel<kE5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHopSmem);
-    if ((e4 ? attr4 : attr5) != cudaSuccess) return cuda_status(e4 ? attr4 : attr5);
-    static int resident4 = resident_blocks(ring_hop_kernel<kE4M3>, kHopThreads, kHopSmem);
-    static int resident5 = resident_blocks(ring_hop_kernel<kE5M2>, kHopThreads, kHopSmem);
-    const unsigned grid = grid_for((size_t)start, e4 ? resident4 : resident5);
-    if (e4)
-        ring_hop_kernel<kE4M3><<<grid, kHopThreads, kHopSmem, stream>>>(g);
-    else
-        ring_hop_kernel<kE5M2><<<grid, kHopThreads, kHopSmem, stream>>>(g);
-    return launch_status();
+    const size_t tiles = (size_t)start;
+    if (fmt == FP8Q_E4M3)
+        return requant_bf16 ? launch_hop_kernel<kE4M3, true>(g, tiles, stream)
+                            : launch_hop_kernel<kE4M3, false>(g, tiles, stream);
+    return requant_bf16 ? launch_hop_kernel<kE5M2, true>(g, tiles, stream)
+                        : launch_hop_kernel<kE5M2, false>(g, tiles, stream);
 }
 
 }  // namespace fp8q
@@ -312,4 +318,12 @@ extern "C" fp8q_status_t fp8q_ring_hop(const uint8_t* in_codes, const float* in_
 extern "C" fp8q_status_t fp8q_ring_hop_group(const fp8q_hop_t* hops, int count, fp8q_format_t fmt,
                                              fp8q_stream_t stream) {
     return launch_hops(hops, count, fmt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8q_status_t fp8q_ring_hop_bf16_requant(const uint8_t* in_codes, const float* in_scales,
+                                                    const void* local_bf16, size_t n, fp8q_format_t fmt,
+                                                    uint8_t* out_codes, float* out_scales, void* out_bf16,
+                                                    fp8q_stream_t stream) {
+    const fp8q_hop_t hp = {in_codes, in_scales, local_bf16, n, out_codes, out_scales, out_bf16};
+    return launch_hops(&hp, 1, fmt, reinterpret_cast<cudaStream_t>(stream), true);
 }
