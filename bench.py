@@ -315,24 +315,50 @@ class Workload:
     def run(self, events=None):
         self.sets[0].run(events)
 
+    COPY_LANES = 4                 # side streams per copy direction
+    COPY_PIECE = 32 << 20          # bytes per cudaMemcpyAsync
+
+    def _copy_fanout(self, stream, pairs):
+        """Copies (dst, src) tensor pairs in pieces spread over side streams
+        forked from `stream` and joined back into it, so that several copy
+        engines work on one direction at once."""
+        torch = self.torch
+        key = int(stream.cuda_stream)
+        if not hasattr(self, "_lanes"):
+            self._lanes = {}
+        if key not in self._lanes:
+            self._lanes[key] = [torch.cuda.Stream(self.dev) for _ in range(self.COPY_LANES)]
+        lanes = self._lanes[key]
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for ln in lanes:
+            ln.wait_event(fork)
+        i = 0
+        nbytes = 0
+        for dst, src in pairs:
+            d = dst.reshape(-1)
+            sv = src.reshape(-1)
+            step = max(1, self.COPY_PIECE // d.element_size())
+            for o in range(0, d.numel(), step):
+                with torch.cuda.stream(lanes[i % len(lanes)]):
+                    d[o:o + step].copy_(sv[o:o + step], non_blocking=True)
+                i += 1
+            nbytes += d.numel() * d.element_size()
+        for ln in lanes:
+            join = torch.cuda.Event()
+            join.record(ln)
+            stream.wait_event(join)
+        return nbytes
+
     def h2d(self, ds, stream):
         """Copies the step's inputs from pinned host memory into set `ds`."""
-        with self.torch.cuda.stream(stream):
-            ds.bucket.copy_(self.h_bucket, non_blocking=True)
-            for d, h in zip(ds.layer, self.h_layer):
-                d.copy_(h, non_blocking=True)
-        return self.h_bucket.numel() * 2 + sum(h.numel() * 2 for h in self.h_layer)
+        return self._copy_fanout(stream, [(ds.bucket, self.h_bucket)] + list(zip(ds.layer, self.h_layer)))
 
     def d2h(self, ds, stream):
         """Reads every result of set `ds` back into pinned host memory."""
         if self.h_out is None:
             self.h_out = [self.torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in ds.outputs]
-        nbytes = 0
-        with self.torch.cuda.stream(stream):
-            for h, d in zip(self.h_out, ds.outputs):
-                h.copy_(d, non_blocking=True)
-                nbytes += d.numel() * d.element_size()
-        return nbytes
+        return self._copy_fanout(stream, list(zip(self.h_out, ds.outputs)))
 
     def e2e(self, steps, warmup=2):
         """Steady-state end-to-end throughput of the public API with host
@@ -626,6 +652,67 @@ def ring_sweep(wl, torch, payloads=(64 << 20, 256 << 20), reps=10):
     return out
 
 
+def timed(torch, stream, fn, flush, reps=5):
+    """Mean event time (ms) of fn() on `stream`, L2 flushed before each rep."""
+    fn()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / reps
+
+
+def extra_rows(wl, torch, peak):
+    """The rows beyond the step, each timed on its own on the step's data:
+    the simulated 8-rank FP8 ring AllReduce of the bucket, the MXFP8 receiver
+    (dequantize the layer's expert gate batch), per-tensor scaling."""
+    w, dev, st = wl.w, wl.dev, wl.stream
+    flush = L2Flush(torch, dev)
+    ds = wl.sets[0]
+    P, n = wl.k, wl.n
+    m = n // P
+    parts = [ds.bucket[r] for r in range(P)]
+    res = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    ws = torch.empty(int(w.lib().fp8q_ring_allreduce_workspace_bytes(P, n)), dtype=torch.uint8, device=dev)
+    out = {}
+    wire = [0]
+
+    def ring():
+        wire[0] = w.fp8q_ring_allreduce_sim(parts, "e4m3", results=res, workspace=ws, stream=st)[1]
+    ms = timed(torch, st, ring, flush)
+    kbytes = P * bytes_quantize(m) + (P - 1) * P * bytes_hop(m, False) + P * (n + 4 * nscales(n) + 2 * n)
+    out["ring_allreduce_sim"] = {
+        "ranks": P, "elements": n, "ms": round(ms, 4), "kernel_bytes": kbytes,
+        "GB/s": round(kbytes / (ms * 1e-3) / 1e9, 1), "wire_bytes_per_rank": wire[0],
+        "bf16_ring_bytes_per_rank": 2 * (P - 1) * m * 2,
+        "wire_saving_vs_bf16": round(1 - wire[0] / (2 * (P - 1) * m * 2), 6)}
+    del res, ws
+    name, b, mm, kk = wl.tensors[0]
+    c, sc, sb = ds.mx[0]
+    outw = torch.empty((b, mm, kk), dtype=torch.bfloat16, device=dev)
+    ms = timed(torch, st, lambda: w.mxfp8_dequantize_swizzled(c, sc, out=outw, stream=st), flush)
+    nbytes = 3 * b * mm * kk + sb
+    out["mxfp8_dequantize"] = {"tensor": name, "elements": b * mm * kk, "us": round(1e3 * ms, 2),
+                               "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                               "frac_of_peak": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
+    del outw
+    codes = torch.empty(P * n, dtype=torch.uint8, device=dev)
+    sa = torch.empty(4, dtype=torch.float32, device=dev)
+    x = ds.bucket.reshape(-1)
+    ms = timed(torch, st, lambda: w.fp8q_quantize_tensorwise(x, "e4m3", codes=codes, scale_amax=sa, stream=st), flush)
+    nbytes = 2 * 2 * P * n + P * n                        # two passes over the input, one over the codes
+    out["quantize_tensorwise"] = {"elements": P * n, "us": round(1e3 * ms, 2),
+                                  "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                  "frac_of_peak": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
+    return out
+
+
 # ---------------------------------------------------------------- main ----
 def main():
     ap = argparse.ArgumentParser()
@@ -726,6 +813,7 @@ def main():
         return
 
     peak, peak_kind = measured_peaks()
+    extras = extra_rows(wl, torch, peak)
     total_ms = sum(d["ms"] for d in per_kind.values())
     kernels = {}
     for kind, d in per_kind.items():
@@ -755,9 +843,11 @@ def main():
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
                 "copy_GBps_alone": getattr(wl, "copy_gbps", None),
-                "pipeline": "H2D, kernels and D2H on three streams, two device buffer sets"},
+                "pipeline": "H2D, kernels and D2H on three streams (each copy direction fanned out over 4 "
+                            "side streams in 32 MiB pieces), two device buffer sets"},
         "gpu_launches": nl * steps,
         "fused_vs_naive_reduce": fvn,
+        "next_rows": extras,
         "ring_hop_sweep": {k: dict(v, frac_of_peak=round(v["GB/s"] / peak, 4)) for k, v in sweep.items()},
         "clocks": clock_info,
         "cpu_baseline": None,
