@@ -161,19 +161,19 @@ def kernel_source_hash(name):
 
 
 def ncu_traffic(name):
-    """DRAM bytes per launch from the committed ncu summary, only if it was
-    taken on the current source of that kernel (else None)."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.md")
-    if not os.path.exists(p):
-        return None
-    want = f"{name}@{kernel_source_hash(name)}"
-    with open(p) as f:
-        for line in f:
-            if line.startswith("traffic ") and want in line:
-                try:
-                    return float(line.split("=")[1].split()[0])
-                except (IndexError, ValueError):
-                    return None
+    """DRAM bytes per launch from a committed ncu summary (a line
+    `traffic <kernel>@<source hash> = <bytes> ...` in profiles/*.md), only
+    if it was taken on the current source of that kernel (else None)."""
+    import glob
+    want = f"traffic {name}@{kernel_source_hash(name)}"
+    for p in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(p) as f:
+            for line in f:
+                if line.startswith(want):
+                    try:
+                        return float(line.split("=")[1].split()[0])
+                    except (IndexError, ValueError):
+                        return None
     return None
 
 
