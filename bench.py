@@ -177,6 +177,61 @@ def ncu_traffic(name):
     return None
 
 
+# ------------------------------------------------------- host topology ----
+def _cpus(text):
+    """'0-3,8,10-11' -> set of CPU numbers."""
+    out = set()
+    for part in (text or "").split(","):
+        part = part.strip()
+        if not part:
+            continue
+        a, _, b = part.partition("-")
+        out.update(range(int(a), int(b or a) + 1))
+    return out
+
+
+def _cpu_text(cpus):
+    cpus = sorted(cpus)
+    runs, i = [], 0
+    while i < len(cpus):
+        j = i
+        while j + 1 < len(cpus) and cpus[j + 1] == cpus[j] + 1:
+            j += 1
+        runs.append(str(cpus[i]) if i == j else f"{cpus[i]}-{cpus[j]}")
+        i = j + 1
+    return ",".join(runs)
+
+
+def bind_to_gpu_numa(torch, dev):
+    """Restricts this process to the CPUs local to the GPU (sysfs
+    local_cpulist of its PCI function) when they are among the CPUs it may
+    use, before any pinned host buffer is allocated, so that the buffers are
+    placed on the GPU's side of the host.  Returns what it found and did."""
+    p = torch.cuda.get_device_properties(dev)
+    bdf = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    info = {"gpu_pci": bdf}
+
+    def read(name):
+        try:
+            with open(os.path.join("/sys/bus/pci/devices", bdf, name)) as f:
+                return f.read().strip()
+        except OSError:
+            return None
+
+    info["gpu_numa_node"] = read("numa_node")
+    local = _cpus(read("local_cpulist"))
+    allowed = os.sched_getaffinity(0)
+    info["allowed_cpus"] = _cpu_text(allowed)
+    info["gpu_local_cpus"] = _cpu_text(local) if local else None
+    both = allowed & local
+    if both and both != allowed:
+        os.sched_setaffinity(0, both)
+        info["bound_to"] = _cpu_text(both)
+    else:
+        info["bound_to"] = None
+    return info
+
+
 # ------------------------------------------------------------- L2 flush ----
 class L2Flush:
     """Evicts L2 between timed steps: writes a buffer larger than L2, then
@@ -244,13 +299,19 @@ class DeviceSet:
             ob, of = self.red[f]
             add("dequant_reduce_kernel", bytes_reduce(n, k), n, L.fp8q_dequant_reduce, cp, sp, ctypes.c_int(k),
                 ctypes.c_size_t(n), ctypes.c_int(f), vp(ob.data_ptr()), vp(of.data_ptr()), sp_)
-        prev = (self.q[0][0][0], self.q[0][1][0])        # hop 0 = e4m3 quantize of rank 0's shard
+        # hop 0 = e4m3 quantize of rank 0's shard; hop h adds shard h, which
+        # only the step's input copy writes, so each hop may start reading it
+        # while the previous hop drains
+        prev = (self.q[0][0][0], self.q[0][1][0])
         for h in range(1, k):
             oc, osc = self.hops[h - 1]
             last = h == k - 1
-            add("ring_hop_kernel", bytes_hop(n, last), n, L.fp8q_ring_hop, vp(prev[0].data_ptr()),
-                vp(prev[1].data_ptr()), vp(self.bucket[h].data_ptr()), ctypes.c_size_t(n), ctypes.c_int(0),
-                vp(oc.data_ptr()), vp(osc.data_ptr()), vp(self.ring_bf16.data_ptr() if last else None), sp_)
+            hp = (wl.w.fp8q_hop_t * 1)(wl.w.fp8q_hop_t(prev[0].data_ptr(), prev[1].data_ptr(),
+                                                        self.bucket[h].data_ptr(), n, oc.data_ptr(),
+                                                        osc.data_ptr(), self.ring_bf16.data_ptr() if last else None))
+            self._keep.append(hp)
+            add("ring_hop_kernel", bytes_hop(n, last), n, L.fp8q_ring_hop_group_ex, hp, ctypes.c_int(1),
+                ctypes.c_int(0), ctypes.c_uint(wl.w.FP8Q_HOP_LOCAL_READY), sp_)
             prev = (oc, osc)
         # the whole layer (expert batches and attention matrices) in one launch
         self._group = (wl.w.mxfp8_tensor_t * len(wl.tensors))()
@@ -263,16 +324,40 @@ class DeviceSet:
             ctypes.c_int(len(wl.tensors)), sp_)
         self.launches = launches
 
-    def run(self, events=None):
+    def segments(self):
+        """Runs of consecutive launches of one kernel: (kind, first, last)."""
+        runs = []
+        for i, (kind, _, _, _, _) in enumerate(self.launches):
+            if runs and runs[-1][0] == kind:
+                runs[-1][2] = i
+            else:
+                runs.append([kind, i, i])
+        return [tuple(r) for r in runs]
+
+    def run(self, events=None, only=None, segments=False):
         """Launch one step on this set's stream; with `events`, bracket each
-        launch with a pair of timing events."""
-        for i, (_, _, _, fn, args) in enumerate(self.launches):
-            if events is not None:
+        launch (or, with `only`, each launch of that kernel; with `segments`,
+        each run of launches of one kernel) with a pair of timing events.  An
+        event between two launches also ends the overlap of the second with
+        the first, so the timed steps bracket only the kernel whose roofline
+        is reported."""
+        starts = ends = None
+        if segments:
+            runs = self.segments()
+            starts, ends = {r[1] for r in runs}, {r[2] for r in runs}
+        for i, (kind, _, _, fn, args) in enumerate(self.launches):
+            if events is None:
+                before = after = False
+            elif segments:
+                before, after = i in starts, i in ends
+            else:
+                before = after = only is None or kind == only
+            if before:
                 events[2 * i].record(self.stream)
             st = fn(*args)
             if st != 0:
                 raise RuntimeError(f"launch {i} failed with status {st}")
-            if events is not None:
+            if after:
                 events[2 * i + 1].record(self.stream)
 
 
@@ -312,8 +397,8 @@ class Workload:
     def red(self):
         return self.sets[0].red
 
-    def run(self, events=None):
-        self.sets[0].run(events)
+    def run(self, events=None, only=None, segments=False):
+        self.sets[0].run(events, only, segments)
 
     COPY_LANES = 4                 # side streams per copy direction
     COPY_PIECE = 32 << 20          # bytes per cudaMemcpyAsync
@@ -387,6 +472,21 @@ class Workload:
                 torch.cuda.synchronize(self.dev)
                 best = max(best, nb / (a.elapsed_time(b) * 1e-3) / 1e9)
             self.copy_gbps[name] = round(best, 1)
+        # both directions at once (step i+1's inputs in while step i's results
+        # go out): the pipeline's ceiling when the host side is shared
+        best = 0.0
+        for _ in range(3):
+            a, b, c = Ev(enable_timing=True), Ev(enable_timing=True), Ev(enable_timing=True)
+            torch.cuda.synchronize(self.dev)
+            a.record(s_in)
+            s_out.wait_event(a)
+            nb_in = self.h2d(self.sets[0], s_in)
+            nb_out = self.d2h(self.sets[1], s_out)
+            b.record(s_in)
+            c.record(s_out)
+            torch.cuda.synchronize(self.dev)
+            best = max(best, (nb_in + nb_out) / (max(a.elapsed_time(b), a.elapsed_time(c)) * 1e-3) / 1e9)
+        self.copy_gbps["both"] = round(best, 1)
         bi = bo = 0
         total = warmup + steps
         done_run = [None, None]      # compute of the set's previous step finished (inputs free)
@@ -749,6 +849,7 @@ def main():
         if world > 1:
             dist.barrier()
 
+    topo = bind_to_gpu_numa(torch, dev)
     wl = Workload(dev, rank, torch)
     flush = L2Flush(torch, dev)
     warmup = max(args.warmup, 3)
@@ -765,6 +866,40 @@ def main():
     clocks.start()
     time.sleep(0.05)
 
+    # ---------------- per-kernel breakdown (before the timed region) ------
+    # every launch bracketed by events: the share of each kernel and the
+    # kernel whose roofline is reported
+    nbreak = min(steps, 50)
+    break_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)] for _ in range(nbreak)]
+    for i in range(nbreak):
+        flush()
+        wl.run(break_ev[i])
+    torch.cuda.synchronize()
+    per_kind = {}
+    for i in range(nbreak):
+        for j, (kind, nbytes, elems, _, _) in enumerate(wl.launches):
+            dt = break_ev[i][2 * j].elapsed_time(break_ev[i][2 * j + 1])
+            d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "bytes": 0, "elems": 0})
+            d["launches"] += 1
+            d["ms"] += dt
+            d["bytes"] += nbytes
+            d["elems"] += elems
+    dom = max(per_kind, key=lambda k: per_kind[k]["ms"])
+
+    # each run of launches of one kernel timed as a whole: inside a run the
+    # launches overlap as they do in the timed steps (no event between them)
+    seg_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)] for _ in range(nbreak)]
+    for i in range(nbreak):
+        flush()
+        wl.run(seg_ev[i], segments=True)
+    torch.cuda.synchronize()
+    segments = []
+    for kind, a, b in wl.sets[0].segments():
+        ms = sum(seg_ev[i][2 * a].elapsed_time(seg_ev[i][2 * b + 1]) for i in range(nbreak)) / nbreak
+        nbytes = sum(wl.launches[j][1] for j in range(a, b + 1))
+        segments.append({"kernel": kind, "launches": b - a + 1, "us": round(1e3 * ms, 2),
+                         "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)})
+
     # ---------------- timed region: K device-resident steps ----------------
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     launch_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)] for _ in range(steps)]
@@ -774,7 +909,7 @@ def main():
     for i in range(steps):
         flush()                                     # evict L2 between steps
         step_ev[i][0].record(wl.stream)
-        wl.run(launch_ev[i])
+        wl.run(launch_ev[i], only=dom)
         step_ev[i][1].record(wl.stream)
     torch.cuda.synchronize()
     barrier()
@@ -783,15 +918,26 @@ def main():
 
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     ms_local = sum(step_ms) / steps
-    per_kind = {}
+    dom_ms, dom_launches = 0.0, 0
     for i in range(steps):
-        for j, (kind, nbytes, elems, _, _) in enumerate(wl.launches):
-            dt = launch_ev[i][2 * j].elapsed_time(launch_ev[i][2 * j + 1])
-            d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "bytes": 0, "elems": 0})
-            d["launches"] += 1
-            d["ms"] += dt
-            d["bytes"] += nbytes
-            d["elems"] += elems
+        for j, (kind, _, _, _, _) in enumerate(wl.launches):
+            if kind == dom:
+                dom_ms += launch_ev[i][2 * j].elapsed_time(launch_ev[i][2 * j + 1])
+                dom_launches += 1
+    dom_bytes = per_kind[dom]["bytes"] // per_kind[dom]["launches"]
+
+    # the same steps with programmatic dependent launch switched off
+    wl.w.fp8q_set_launch_overlap(False)
+    noov_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nbreak)]
+    for i in range(nbreak):
+        flush()
+        noov_ev[i][0].record(wl.stream)
+        wl.run()
+        noov_ev[i][1].record(wl.stream)
+    torch.cuda.synchronize()
+    wl.w.fp8q_set_launch_overlap(True)
+    ms_no_overlap = sum(a.elapsed_time(b) for a, b in noov_ev) / nbreak
+
     ms_step, bytes_all, elems_all = combine_over_ranks(dist if world > 1 else None, dev, ms_local,
                                                        float(wl.step_bytes), float(wl.step_elems))
     value_gbs = bytes_all / (ms_step * 1e-3) / 1e9
@@ -819,12 +965,10 @@ def main():
     for kind, d in per_kind.items():
         avg_ms = d["ms"] / d["launches"]
         gbs = d["bytes"] / (d["ms"] * 1e-3) / 1e9
-        kernels[kind] = {"launches_per_step": d["launches"] // steps, "avg_us": round(1e3 * avg_ms, 2),
+        kernels[kind] = {"launches_per_step": d["launches"] // nbreak, "avg_us": round(1e3 * avg_ms, 2),
                          "bytes_per_launch": d["bytes"] // d["launches"], "GB/s": round(gbs, 1),
                          "frac_of_peak": round(gbs / peak, 4), "share": round(d["ms"] / total_ms, 4)}
-    dom = max(per_kind, key=lambda k: per_kind[k]["ms"])
-    dd = per_kind[dom]
-    achieved = dd["bytes"] / (dd["ms"] * 1e-3) / 1e9
+    achieved = dom_bytes * dom_launches / (dom_ms * 1e-3) / 1e9
     traffic = ncu_traffic(dom)
     line = {
         "metric": METRIC, "value": round(value_gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
@@ -838,11 +982,20 @@ def main():
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": f"{peak_kind} HBM copy GB/s", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": dd["bytes"] // dd["launches"]},
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "avg_us": round(1e3 * dom_ms / dom_launches, 2),
+                     "timing": "events around each launch of this kernel in the K timed steps"},
         "kernels": kernels,
+        "kernels_timing": f"separate pass of {nbreak} steps with events around every launch",
+        "segments": [dict(g, frac_of_peak=round(g["GB/s"] / peak, 4)) for g in segments],
+        "segments_timing": f"separate pass of {nbreak} steps with events only where the kernel changes",
+        "launch_overlap": {"step_ms_on": round(ms_local, 4), "step_ms_off": round(ms_no_overlap, 4),
+                           "steps_off": nbreak,
+                           "what": "programmatic dependent launch of every kernel (on in the timed steps)"},
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
                 "copy_GBps_alone": getattr(wl, "copy_gbps", None),
+                "host": topo,
                 "pipeline": "H2D, kernels and D2H on three streams (each copy direction fanned out over 4 "
                             "side streams in 32 MiB pieces), two device buffer sets"},
         "gpu_launches": nl * steps,

@@ -58,7 +58,8 @@ typedef enum {
     FP8Q_ERR_K = 5,      /* shard count outside [1, FP8Q_MAX_SHARDS], or an
                             MXFP8 K that is not a positive multiple of 32     */
     FP8Q_ERR_CUDA = 6,   /* the CUDA runtime rejected a launch                */
-    FP8Q_ERR_ALIAS = 7   /* an output overlaps an input or another output     */
+    FP8Q_ERR_ALIAS = 7,  /* an output overlaps an input or another output     */
+    FP8Q_ERR_FLAGS = 8   /* unknown bits in a flags argument                  */
 } fp8q_status_t;
 
 #define FP8Q_BLOCK 128                   /* elements per blockwise scale   */
@@ -130,6 +131,21 @@ typedef struct {
  * [1, FP8Q_MAX_HOP_GROUP] (FP8Q_ERR_SIZE).  Results are those of one
  * fp8q_ring_hop per hop. */
 fp8q_status_t fp8q_ring_hop_group(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, fp8q_stream_t stream);
+
+/* Flags of fp8q_ring_hop_group_ex. */
+#define FP8Q_HOP_LOCAL_READY 1u
+
+/* fp8q_ring_hop_group with flags (unknown bits: FP8Q_ERR_FLAGS); the results
+ * are those of fp8q_ring_hop_group.
+ * FP8Q_HOP_LOCAL_READY: the caller guarantees that no kernel that can still
+ * be running when this call's kernel starts writes any hop's local_bf16 (in
+ * a ring the local partial is the rank's own gradient bucket, complete before
+ * the incoming chunk arrives).  With programmatic dependent launch on (see
+ * fp8q_set_launch_overlap) the kernel then starts copying the local partials
+ * of its first tiles while the previous kernel on the stream is finishing;
+ * the incoming codes and scales, and every write, still wait for it. */
+fp8q_status_t fp8q_ring_hop_group_ex(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, unsigned int flags,
+                                     fp8q_stream_t stream);
 
 /* ---------------------------------------------------- ring AllReduce ----
  * A ring AllReduce carried on the FP8 wire format, with all P ranks held on
@@ -288,6 +304,16 @@ const char* fp8q_status_string(fp8q_status_t status);
 
 /* cudaError_t of the most recent FP8Q_ERR_CUDA on the calling thread (0 if none). */
 int fp8q_last_cuda_error(void);
+
+/* Programmatic dependent launch, process-wide; on by default.  When on,
+ * every kernel of this library is launched with programmatic stream
+ * serialization: its blocks may be dispatched while the previous kernel on
+ * the stream is still finishing, and each kernel waits on the device for
+ * that kernel to complete, with its writes visible, before it touches global
+ * memory.  Results and stream order are the same either way; only the gap
+ * between dependent launches shrinks.  Returns the previous setting
+ * (1 = on).  Takes effect for launches made after the call. */
+int fp8q_set_launch_overlap(int enable);
 
 /* Diagnostic, and the one call that synchronizes: waits for the current
  * device, then returns in *flags the error bits the kernels raised since the

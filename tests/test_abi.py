@@ -14,7 +14,7 @@ import pytest
 
 from conftest import ROOT, build_lib
 
-OK, ERR_NULL, ERR_SIZE, ERR_ALIGN, ERR_FORMAT, ERR_K, ERR_CUDA, ERR_ALIAS = range(8)
+OK, ERR_NULL, ERR_SIZE, ERR_ALIGN, ERR_FORMAT, ERR_K, ERR_CUDA, ERR_ALIAS, ERR_FLAGS = range(9)
 A = 0x7F0000000000            # a 16-byte aligned fake device address
 MB = 1 << 20
 
@@ -47,10 +47,21 @@ def test_exports_every_declared_function(L):
 
 
 def test_status_strings(L):
-    for s in range(8):
+    for s in range(9):
         assert len(L.fp8q_status_string(s)) > 0
     assert L.fp8q_status_string(0) == b"ok"
     assert L.fp8q_status_string(99) == b"unknown status"
+
+
+def test_launch_overlap_switch(L):
+    # host-only state: on by default, each call returns the previous setting
+    prev = L.fp8q_set_launch_overlap(0)
+    try:
+        assert prev == 1
+        assert L.fp8q_set_launch_overlap(7) == 0
+        assert L.fp8q_set_launch_overlap(1) == 1
+    finally:
+        L.fp8q_set_launch_overlap(prev)
 
 
 def test_size_helpers(L, orc):
@@ -176,6 +187,11 @@ def test_ring_group_and_allreduce_validation(L):
     assert g(two, 2, 0, None) == ERR_ALIAS
     empty = (H * 1)(H(None, None, None, 0, None, None, None))
     assert g(empty, 1, 0, None) == OK
+    gx = L.fp8q_ring_hop_group_ex
+    assert gx(arr, 1, 0, 2, None) == ERR_FLAGS                      # unknown flag bit, checked first
+    assert gx(arr, 1, 0, 0x80000001, None) == ERR_FLAGS
+    assert gx(two, 2, 0, w.FP8Q_HOP_LOCAL_READY, None) == ERR_ALIAS
+    assert gx(empty, 1, 0, w.FP8Q_HOP_LOCAL_READY, None) == OK
     assert L.fp8q_ring_allreduce_workspace_bytes(8, 13_107_200) > 0
     assert L.fp8q_ring_allreduce_workspace_bytes(8, 1000) == 0
     assert L.fp8q_ring_allreduce_workspace_bytes(1, 1024) == 0

@@ -105,3 +105,41 @@ def test_ring_chain_large_sampled(w, orc, payload):
             c, s, bf = orc.ring_hop(c, s, hb[h][sl].copy(), 0)
         assert_same(gpu_codes[-1][sl], c, f"block {b} final")
         assert_same(gpu_last[sl], bf, f"block {b} bf16")
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("want_bf16", [True, False])
+def test_hop_signed_zeros_and_cancellation(w, orc, fmt, want_bf16):
+    # power-of-two block scales make every dequantized value exact in bf16,
+    # so the local partial can cancel it exactly: sums of +0 from opposite
+    # signs, -0 + -0, all-zero blocks after cancellation, zero scales,
+    # subnormal sums and near-cancellation, over a ragged tail
+    rng = np.random.default_rng(321 + fmt)
+    nb = 96
+    n = nb * 128 - 45
+    codes = rng.integers(0, 256, n, dtype=np.uint8)
+    nan_bits = 0x7F if fmt == 0 else 0x7C
+    codes[(codes & nan_bits) == nan_bits] = 0x23
+    kind = np.arange(nb) % 6
+    scales = np.ldexp(np.float32(1.0), rng.integers(-60, 60, nb)).astype(np.float32)
+    scales[kind == 3] = 0.0
+    scales[kind == 4] = np.float32(2.0 ** -140)
+    ek = np.repeat(kind, 128)[:n]
+    zc = ek == 1
+    codes[zc] = np.where(rng.random(zc.sum()) < 0.5, 0x00, 0x80).astype(np.uint8)
+    a = orc.dequantize(codes, scales, fmt)[1]
+    sz = np.where(rng.random(n) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+    loc = np.where(ek == 0, -a, sz)
+    half = (ek == 2) & (rng.random(n) < 0.5)
+    loc = np.where(half, -a, np.where(ek == 2, rng.standard_normal(n).astype(np.float32) * np.abs(a), loc))
+    loc = np.where(ek == 5, -a * np.float32(1.0078125), loc)
+    lb = orc.f32_to_bf16(loc.astype(np.float32))
+    assert np.array_equal(orc.bf16_to_f32(lb)[ek == 0], -a[ek == 0])      # the cancellation is exact
+    dc, ds = torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda()
+    oc, os_, ob = w.fp8q_ring_hop(dc, ds, bf16_from_bits(lb), fmt, want_bf16=want_bf16)
+    ec, es, eb = orc.ring_hop(codes, scales, lb, fmt)
+    assert np.signbit(orc.bf16_to_f32(eb)).any() and (eb == 0).any()      # both zero signs occur
+    assert_same_f32(os_.cpu().numpy(), es, "scales")
+    assert_same(u8(oc), ec, "codes")
+    if want_bf16:
+        assert_same(bits16(ob), eb, "bf16")

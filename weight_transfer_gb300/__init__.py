@@ -54,6 +54,7 @@ class fp8q_hop_t(ctypes.Structure):
 
 
 FP8Q_MAX_HOP_GROUP = 16
+FP8Q_HOP_LOCAL_READY = 1
 
 
 class mxfp8_tensor_t(ctypes.Structure):
@@ -95,6 +96,7 @@ _SIGNATURES = {
                         ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(_int)], _int),
     "fp8q_copy_segments": ([ctypes.POINTER(fp8q_copy_t), _int, _vp], _int),
     "fp8q_ring_hop_group": ([ctypes.POINTER(fp8q_hop_t), _int, _int, _vp], _int),
+    "fp8q_ring_hop_group_ex": ([ctypes.POINTER(fp8q_hop_t), _int, _int, ctypes.c_uint, _vp], _int),
     "fp8q_ring_allreduce_workspace_bytes": ([_int, _sz], _sz),
     "fp8q_ring_allreduce_sim": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _sz,
                                  ctypes.POINTER(ctypes.c_uint64), _vp], _int),
@@ -102,6 +104,7 @@ _SIGNATURES = {
     "mxfp8_swizzled_scale_bytes": ([_i64, _i64, _i64], _sz),
     "fp8q_status_string": ([_int], ctypes.c_char_p),
     "fp8q_last_cuda_error": ([], _int),
+    "fp8q_set_launch_overlap": ([_int], _int),
     "fp8q_device_errors": ([ctypes.POINTER(ctypes.c_uint), _int], _int),
     "fp8q_encode_f32": ([_vp, _sz, _int, _vp, _vp], _int),
     "fp8q_dequantize": ([_vp, _vp, _sz, _int, _vp, _vp, _vp], _int),
@@ -173,6 +176,12 @@ def fp8q_device_errors(clear: bool = True) -> int:
     v = ctypes.c_uint(0)
     _check("fp8q_device_errors", lib().fp8q_device_errors(ctypes.byref(v), int(clear)))
     return int(v.value)
+
+
+def fp8q_set_launch_overlap(enable: bool) -> bool:
+    """Switches programmatic dependent launch for every later launch of the
+    library (on by default); returns the previous setting."""
+    return bool(lib().fp8q_set_launch_overlap(1 if enable else 0))
 
 
 def fp8q_num_scales(n: int) -> int:
@@ -275,6 +284,12 @@ def fp8q_ring_hop_group(hops: Sequence[dict], fmt="e4m3", stream=None):
     in_codes, in_scales, local and optionally out_codes, out_scales,
     out_bf16 (allocated when missing; out_bf16 only if want_bf16).  Returns
     the list of (out_codes, out_scales, out_bf16 or None)."""
+    return fp8q_ring_hop_group_ex(hops, fmt, 0, stream, _name="fp8q_ring_hop_group")
+
+
+def fp8q_ring_hop_group_ex(hops: Sequence[dict], fmt="e4m3", flags: int = 0, stream=None, _name=None):
+    """fp8q_ring_hop_group with flags (FP8Q_HOP_LOCAL_READY: no kernel still
+    running when this launch starts writes any hop's local partial)."""
     count = len(hops)
     arr = (fp8q_hop_t * max(count, 1))()
     outs = []
@@ -297,7 +312,12 @@ def fp8q_ring_hop_group(hops: Sequence[dict], fmt="e4m3", stream=None):
                             _dev(os_, f"hops[{i}].out_scales", torch.float32, nb),
                             _dev(ob, f"hops[{i}].out_bf16", torch.bfloat16, n))
         outs.append((oc, os_, ob))
-    _check("fp8q_ring_hop_group", lib().fp8q_ring_hop_group(arr, count, _fmt(fmt), _stream(stream)))
+    if _name == "fp8q_ring_hop_group":
+        st = lib().fp8q_ring_hop_group(arr, count, _fmt(fmt), _stream(stream))
+    else:
+        _name = "fp8q_ring_hop_group_ex"
+        st = lib().fp8q_ring_hop_group_ex(arr, count, _fmt(fmt), flags, _stream(stream))
+    _check(_name, st)
     return outs
 
 

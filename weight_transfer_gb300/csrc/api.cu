@@ -2,9 +2,14 @@
 // CUDA error capture and the cached device query used for launch sizing.
 #include "fp8q_host.cuh"
 
+#include <atomic>
+
 namespace fp8q {
 
 static thread_local int g_last_cuda_error = 0;
+static std::atomic<int> g_launch_overlap{1};
+
+bool launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
 
 fp8q_status_t cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return FP8Q_OK;
@@ -27,6 +32,10 @@ int sm_count() {
 
 extern "C" size_t fp8q_num_scales(size_t n) { return n / FP8Q_BLOCK + (n % FP8Q_BLOCK != 0); }
 
+extern "C" int fp8q_set_launch_overlap(int enable) {
+    return fp8q::g_launch_overlap.exchange(enable != 0 ? 1 : 0);
+}
+
 extern "C" int fp8q_last_cuda_error(void) { return fp8q::g_last_cuda_error; }
 
 extern "C" const char* fp8q_status_string(fp8q_status_t status) {
@@ -39,6 +48,7 @@ extern "C" const char* fp8q_status_string(fp8q_status_t status) {
         case FP8Q_ERR_K: return "shard count or MXFP8 K out of range";
         case FP8Q_ERR_CUDA: return "CUDA launch error (see fp8q_last_cuda_error)";
         case FP8Q_ERR_ALIAS: return "an output overlaps an input or another output";
+        case FP8Q_ERR_FLAGS: return "unknown bits in a flags argument";
     }
     return "unknown status";
 }

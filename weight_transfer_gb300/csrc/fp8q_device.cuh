@@ -96,6 +96,18 @@ __device__ __forceinline__ void decode_fp8x4(uint32_t w, float* f) {
     f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
+// -------------------------------------------- programmatic dependent launch ----
+// Every kernel of the library is launched so that it may be dispatched while
+// the previous kernel on its stream is still finishing.  A kernel calls
+// dependency_wait() before its first global-memory access: the wait returns
+// once the preceding grid has completed and its writes are visible (at once
+// when the launch had no such overlap).  allow_dependents() right after it
+// lets the next launch's blocks take SM slots as this grid's blocks retire;
+// they only fit as this grid drains, so the overlap covers launch, block
+// dispatch and the shared-memory prologue, never data.
+__device__ __forceinline__ void dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------- memory access ----
 // Streaming 16-byte load through the read-only path without L1 allocation:
 // every byte is read once.

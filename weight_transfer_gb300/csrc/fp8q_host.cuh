@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "fp8q.h"
 
 namespace fp8q {
@@ -51,6 +53,30 @@ inline unsigned grid_for(size_t work_blocks, int resident) {
     size_t cap = (size_t)sm_count() * (size_t)(resident > 0 ? resident : 1);
     size_t g = work_blocks < cap ? work_blocks : cap;
     return (unsigned)(g > 0 ? g : 1);
+}
+
+// Process-wide switch of programmatic dependent launch (fp8q_set_launch_overlap).
+bool launch_overlap();
+
+// Launches `kernel` on `stream`, with programmatic stream serialization when
+// the switch is on (the kernel then waits on the device for its predecessor,
+// see dependency_wait), and returns the launch status.
+template <typename... KArgs, typename... Args>
+fp8q_status_t launch(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = launch_overlap() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) (void)cudaGetLastError();     // leave no error behind for later launches
+    return cuda_status(e);
 }
 
 }  // namespace fp8q

@@ -84,6 +84,8 @@ mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
         for (int s = 0; s < kMxStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
+    dependency_wait();
+    allow_dependents();
     __syncthreads();
     auto issue = [&](int64_t t, int s) {          // thread 0 only
         const int gi = group_of(g, t);
@@ -289,8 +291,7 @@ static fp8q_status_t launch_group(const mxfp8_tensor_t* tensors, int count, cuda
     if (attr != cudaSuccess) return cuda_status(attr);
     static int resident = resident_blocks(mxfp8_quantize_kernel, kMxThreads, kMxSmem);
     const unsigned grid = grid_for((size_t)start, resident);
-    mxfp8_quantize_kernel<<<grid, kMxThreads, kMxSmem, stream>>>(g);
-    return launch_status();
+    return launch(mxfp8_quantize_kernel, grid, kMxThreads, kMxSmem, stream, g);
 }
 
 }  // namespace fp8q

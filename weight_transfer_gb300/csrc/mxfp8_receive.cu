@@ -26,6 +26,8 @@ __device__ __forceinline__ int64_t swizzle_offset(int64_t bt, int64_t r, int64_t
 __global__ void __launch_bounds__(256)
 mxfp8_dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int64_t m,
                         int64_t k, size_t units, uint16_t* __restrict__ out) {
+    dependency_wait();
+    allow_dependents();
     const int64_t kb = k / 32;
     for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (size_t)gridDim.x * blockDim.x) {
         const size_t e0 = u * 16;
@@ -53,6 +55,8 @@ mxfp8_dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __rest
 __global__ void __launch_bounds__(256)
 mxfp8_unswizzle_kernel(const uint8_t* __restrict__ scales, int64_t m, int64_t kb, size_t total,
                        uint8_t* __restrict__ out) {
+    dependency_wait();
+    allow_dependents();
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
         const int64_t j = (int64_t)(i % (size_t)kb);
         const int64_t row = (int64_t)(i / (size_t)kb);
@@ -65,6 +69,8 @@ mxfp8_unswizzle_kernel(const uint8_t* __restrict__ scales, int64_t m, int64_t kb
 __global__ void __launch_bounds__(256)
 count_mismatches_kernel(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b, size_t n,
                         unsigned long long* count) {
+    dependency_wait();
+    allow_dependents();
     unsigned long long mine = 0;
     const size_t n16 = n / 16;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -104,9 +110,9 @@ extern "C" fp8q_status_t mxfp8_dequantize_swizzled(const uint8_t* codes, const u
     if (overlaps(out_bf16, 2 * n, codes, n) || overlaps(out_bf16, 2 * n, scales_swizzled, sb)) return FP8Q_ERR_ALIAS;
     static int resident = resident_blocks(mxfp8_dequantize_kernel, 256);
     const size_t units = n / 16;
-    mxfp8_dequantize_kernel<<<grid_for((units + 255) / 256, resident), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        codes, scales_swizzled, m, k, units, static_cast<uint16_t*>(out_bf16));
-    return launch_status();
+    return launch(mxfp8_dequantize_kernel, grid_for((units + 255) / 256, resident), 256, 0,
+                  reinterpret_cast<cudaStream_t>(stream), codes, scales_swizzled, m, k, units,
+                  static_cast<uint16_t*>(out_bf16));
 }
 
 extern "C" fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, int64_t batch, int64_t m, int64_t k,
@@ -120,9 +126,9 @@ extern "C" fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, 
     if (overlaps(scales_rowmajor, total, scales_swizzled, mxfp8_swizzled_scale_bytes(batch, m, k)))
         return FP8Q_ERR_ALIAS;
     static int resident = resident_blocks(mxfp8_unswizzle_kernel, 256);
-    mxfp8_unswizzle_kernel<<<grid_for((total + 255) / 256, resident), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        scales_swizzled, m, k / MXFP8_BLOCK, total, scales_rowmajor);
-    return launch_status();
+    return launch(mxfp8_unswizzle_kernel, grid_for((total + 255) / 256, resident), 256, 0,
+                  reinterpret_cast<cudaStream_t>(stream), scales_swizzled, m, (int64_t)(k / MXFP8_BLOCK), total,
+                  scales_rowmajor);
 }
 
 extern "C" fp8q_status_t fp8q_count_mismatches(const void* a, const void* b, size_t nbytes, unsigned long long* count,
@@ -133,8 +139,7 @@ extern "C" fp8q_status_t fp8q_count_mismatches(const void* a, const void* b, siz
     if (!aligned16(a) || !aligned16(b) || (reinterpret_cast<uintptr_t>(count) & 7u)) return FP8Q_ERR_ALIGN;
     if (overlaps(count, 8, a, nbytes) || overlaps(count, 8, b, nbytes)) return FP8Q_ERR_ALIAS;
     static int resident = resident_blocks(count_mismatches_kernel, 256);
-    count_mismatches_kernel<<<grid_for((nbytes / 16 + 255) / 256 + 1, resident), 256, 0,
-                              reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<const uint8_t*>(a),
-                                                                         static_cast<const uint8_t*>(b), nbytes, count);
-    return launch_status();
+    return launch(count_mismatches_kernel, grid_for((nbytes / 16 + 255) / 256 + 1, resident), 256, 0,
+                  reinterpret_cast<cudaStream_t>(stream), static_cast<const uint8_t*>(a),
+                  static_cast<const uint8_t*>(b), nbytes, count);
 }

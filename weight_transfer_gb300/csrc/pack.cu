@@ -33,6 +33,8 @@ struct SegmentTable {
 };
 
 __global__ void __launch_bounds__(256) copy_segments_kernel(const __grid_constant__ SegmentTable tab) {
+    dependency_wait();
+    allow_dependents();
     const uint64_t pieces = tab.piece_start[tab.count];
     for (uint64_t p = blockIdx.x; p < pieces; p += gridDim.x) {
         int lo = 0, hi = tab.count - 1;                 // segment with piece_start <= p < next
@@ -120,6 +122,6 @@ extern "C" fp8q_status_t fp8q_copy_segments(const fp8q_copy_t* segs, int count, 
     tab.piece_start[used] = pieces;
     tab.count = used;
     static int resident = resident_blocks(copy_segments_kernel, 256);
-    copy_segments_kernel<<<grid_for((size_t)pieces, resident), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(tab);
-    return launch_status();
+    return launch(copy_segments_kernel, grid_for((size_t)pieces, resident), 256, 0,
+                  reinterpret_cast<cudaStream_t>(stream), tab);
 }

@@ -70,6 +70,8 @@ quantize_blockwise_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __r
         for (int s = 0; s < kQuantStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
+    dependency_wait();
+    allow_dependents();
     __syncthreads();
     auto issue = [&](size_t t, int s) {           // thread 0 only
         mbar_arrive_expect_tx(&full[s], kQuantStageBytes);
@@ -139,6 +141,8 @@ quantize_blockwise_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __r
 template <int FMT>
 __global__ void __launch_bounds__(256)
 encode_f32_kernel(const float* __restrict__ x, size_t n, uint8_t* __restrict__ codes) {
+    dependency_wait();
+    allow_dependents();
     const size_t n4 = n >> 2;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -163,8 +167,7 @@ static fp8q_status_t launch_quantize(const uint16_t* x, size_t n, uint8_t* codes
     static int resident = resident_blocks(quantize_blockwise_kernel<FMT>, kQuantThreads, kQuantSmem);
     const size_t tiles = (n + kQuantTile - 1) / kQuantTile;
     const unsigned grid = grid_for(tiles, resident);
-    quantize_blockwise_kernel<FMT><<<grid, kQuantThreads, kQuantSmem, stream>>>(x, n, codes, scales);
-    return launch_status();
+    return launch(quantize_blockwise_kernel<FMT>, grid, kQuantThreads, kQuantSmem, stream, x, n, codes, scales);
 }
 
 template <int FMT>
@@ -172,8 +175,7 @@ static fp8q_status_t launch_encode(const float* x, size_t n, uint8_t* codes, cud
     static int resident = resident_blocks(encode_f32_kernel<FMT>, 256);
     const size_t units = (n + 3) / 4;
     const unsigned grid = grid_for((units + 255) / 256, resident * 2);
-    encode_f32_kernel<FMT><<<grid, 256, 0, stream>>>(x, n, codes);
-    return launch_status();
+    return launch(encode_f32_kernel<FMT>, grid, 256, 0, stream, x, n, codes);
 }
 
 }  // namespace fp8q

@@ -96,6 +96,8 @@ dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_
         for (int s = 0; s < kRedStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
+    dependency_wait();
+    allow_dependents();
     __syncthreads();
 
     auto issue = [&](size_t t, int s) {           // thread 0 only
@@ -200,6 +202,8 @@ template <bool OUT_BF16, bool OUT_F32>
 __global__ void __launch_bounds__(kRedThreads)
 sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, size_t slot, uint16_t* __restrict__ out_bf16,
                float* __restrict__ out_f32) {
+    dependency_wait();
+    allow_dependents();
     const size_t units = (n + 15) >> 4;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
@@ -243,8 +247,7 @@ static fp8q_status_t launch_reduce_k(const ShardPtrs& sh, int k, size_t n, uint1
     if (resident[k] == 0) resident[k] = resident_blocks(kernel, kRedThreads, smem);
     const size_t tiles = (n + kRedTile - 1) / kRedTile;
     const unsigned grid = grid_for(tiles, resident[k]);
-    kernel<<<grid, kRedThreads, smem, s>>>(sh, k, n, ob, of);
-    return launch_status();
+    return launch(kernel, grid, kRedThreads, smem, s, sh, k, n, ob, of);
 }
 
 template <int FMT, bool B, bool F, bool SUM>
@@ -272,8 +275,7 @@ static fp8q_status_t launch_sum_t(const float* ws, int k, size_t n, size_t strid
     static int resident = resident_blocks(sum_f32_kernel<B, F>, kRedThreads);
     const size_t units = (n + 15) / 16;
     const unsigned grid = grid_for((units + kRedThreads - 1) / kRedThreads, resident);
-    sum_f32_kernel<B, F><<<grid, kRedThreads, 0, s>>>(ws, k, n, stride, ob, of);
-    return launch_status();
+    return launch(sum_f32_kernel<B, F>, grid, kRedThreads, 0, s, ws, k, n, stride, ob, of);
 }
 
 // Shared argument checks of the multi-shard entry points.

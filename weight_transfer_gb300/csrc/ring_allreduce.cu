@@ -116,7 +116,11 @@ extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, vo
             }
             hp.out_bf16 = nullptr;
         }
-        const fp8q_status_t st = fp8q_ring_hop_group(hops, ranks, fmt, stream);
+        // The local partials are the callers' inputs: no kernel of this call
+        // writes them, and whatever wrote them had finished before the first
+        // quantize above passed its grid-dependency wait, so each hop group
+        // may start reading them while the previous group drains.
+        const fp8q_status_t st = fp8q_ring_hop_group_ex(hops, ranks, fmt, FP8Q_HOP_LOCAL_READY, stream);
         if (st != FP8Q_OK) return st;
     }
     // all-gather of the reduced codes, then every rank decodes the whole vector

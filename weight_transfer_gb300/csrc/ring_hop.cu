@@ -16,9 +16,13 @@
 // elements [8j, 8j+8) and [64+8j, 64+8j+8) (conflict-free shared-memory
 // reads), the amax is a 3-step xor-shuffle among the 8 lanes, and the
 // quotients y / s use the per-block reciprocal with two Markstein
-// corrections (exact for binary32 dividends, see block_quotients).  The sums
-// stay in registers from the add to the requantization.  The ragged last
-// tile is read straight from global memory.
+// corrections (exact for binary32 dividends, see block_quotients).  The
+// sums stay in registers from the add to the requantization.  The ragged last tile is
+// read straight from global memory.
+//
+// With FP8Q_HOP_LOCAL_READY the local partials of each CTA's first tiles are
+// copied before the grid-dependency wait, so that they stream in while the
+// previous kernel on the stream drains.
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
@@ -49,6 +53,7 @@ struct HopGroup {
     size_t n[kHopMaxGroup];
     int64_t tile_start[kHopMaxGroup + 1];
     int count;
+    int local_ready;       // the local partials may be read before the predecessor grid ends
 };
 
 // REQ_BF16: requantize RNE_bf16(y), the bf16 partial a receiver keeps,
@@ -73,16 +78,21 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
         for (int s = 0; s < kHopStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
-    __syncthreads();
     // a tile is staged through shared memory when it lies entirely inside its hop's arrays
     auto staged_tile = [&](int64_t t, int h) { return (size_t)(t - g.tile_start[h] + 1) * kHopTile <= g.n[h]; };
-    auto issue = [&](int64_t t, int h, int s) {   // thread 0 only
+    // arms stage s for a whole tile and copies the tile's local partial
+    auto issue_local = [&](int64_t t, int h, int s) {   // thread 0 only
         const size_t lt = (size_t)(t - g.tile_start[h]);
         uint8_t* st = smem + (size_t)s * kHopStageBytes;
         mbar_arrive_expect_tx(&full[s], kHopStageBytes);
+        bulk_g2s(st + kHopCodesBytes + kHopScaleBytes, g.local[h] + lt * kHopTile, kHopLocalBytes, &full[s]);
+    };
+    // the incoming codes and scales of the tile (the rest of the stage's bytes)
+    auto issue_incoming = [&](int64_t t, int h, int s) {   // thread 0 only
+        const size_t lt = (size_t)(t - g.tile_start[h]);
+        uint8_t* st = smem + (size_t)s * kHopStageBytes;
         bulk_g2s(st, g.in_codes[h] + lt * kHopTile, kHopCodesBytes, &full[s]);
         bulk_g2s(st + kHopCodesBytes, g.in_scales[h] + lt * kHopTileBlocks, kHopScaleBytes, &full[s]);
-        bulk_g2s(st + kHopCodesBytes + kHopScaleBytes, g.local[h] + lt * kHopTile, kHopLocalBytes, &full[s]);
     };
     // A hop's ragged last tile is not staged and can sit between staged tiles,
     // so each stage's barrier parity is tracked explicitly: bit s of `parity`
@@ -91,13 +101,30 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
     // copy issued and not yet consumed.
     uint32_t parity = 0;
     uint32_t pending = 0;
+    // the first tiles' local partials, before the predecessor grid has ended,
+    // when the caller guarantees that it does not write them
+    if (tid == 0 && g.local_ready)
+        for (int s = 0; s < kHopStages; ++s) {
+            const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+            if (t < total_tiles) {
+                const int h = hop_of(t);
+                if (staged_tile(t, h)) {
+                    issue_local(t, h, s);
+                    pending |= 1u << s;
+                }
+            }
+        }
+    dependency_wait();
+    allow_dependents();
+    __syncthreads();
     if (tid == 0)
         for (int s = 0; s < kHopStages; ++s) {
             const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
             if (t < total_tiles) {
                 const int h = hop_of(t);
                 if (staged_tile(t, h)) {
-                    issue(t, h, s);
+                    if (!g.local_ready) issue_local(t, h, s);
+                    issue_incoming(t, h, s);
                     pending |= 1u << s;
                 }
             }
@@ -138,13 +165,14 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
             s_in = b < nb ? g.in_scales[h][b] : 0.0f;
         }
 
-        float d[16], lf[16], y[16];
+        float d[16], lf[16];
         decode_fp8x4<FMT>(ca.x, d);
         decode_fp8x4<FMT>(ca.y, d + 4);
         decode_fp8x4<FMT>(cb.x, d + 8);
         decode_fp8x4<FMT>(cb.y, d + 12);
         unpack8(la, *reinterpret_cast<float(*)[8]>(lf));
         unpack8(lb, *reinterpret_cast<float(*)[8]>(lf + 8));
+        float y[16];
         float a = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -196,7 +224,8 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
                 const int hn = hop_of(tn);
                 if (staged_tile(tn, hn)) {
                     fence_proxy_async_smem();
-                    issue(tn, hn, s);
+                    issue_local(tn, hn, s);
+                    issue_incoming(tn, hn, s);
                     pending |= 1u << s;
                 }
             }
@@ -239,12 +268,12 @@ static fp8q_status_t launch_hop_kernel(const HopGroup& g, size_t tiles, cudaStre
                                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHopSmem);
     if (attr != cudaSuccess) return cuda_status(attr);
     static int resident = resident_blocks(ring_hop_kernel<FMT, REQ>, kHopThreads, kHopSmem);
-    ring_hop_kernel<FMT, REQ><<<grid_for(tiles, resident), kHopThreads, kHopSmem, stream>>>(g);
-    return launch_status();
+    return launch(ring_hop_kernel<FMT, REQ>, grid_for(tiles, resident), kHopThreads, kHopSmem, stream, g);
 }
 
 static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, cudaStream_t stream,
-                                 bool requant_bf16 = false) {
+                                 bool requant_bf16 = false, unsigned flags = 0) {
+    if (flags & ~FP8Q_HOP_LOCAL_READY) return FP8Q_ERR_FLAGS;
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
     if (!hops) return FP8Q_ERR_NULL;
     if (count < 1 || count > kHopMaxGroup) return FP8Q_ERR_SIZE;
@@ -292,6 +321,7 @@ static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_
     if (used == 0) return FP8Q_OK;
     g.tile_start[used] = start;
     g.count = used;
+    g.local_ready = (flags & FP8Q_HOP_LOCAL_READY) ? 1 : 0;
     const size_t tiles = (size_t)start;
     if (fmt == FP8Q_E4M3)
         return requant_bf16 ? launch_hop_kernel<kE4M3, true>(g, tiles, stream)
@@ -318,6 +348,11 @@ extern "C" fp8q_status_t fp8q_ring_hop(const uint8_t* in_codes, const float* in_
 extern "C" fp8q_status_t fp8q_ring_hop_group(const fp8q_hop_t* hops, int count, fp8q_format_t fmt,
                                              fp8q_stream_t stream) {
     return launch_hops(hops, count, fmt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8q_status_t fp8q_ring_hop_group_ex(const fp8q_hop_t* hops, int count, fp8q_format_t fmt,
+                                                unsigned int flags, fp8q_stream_t stream) {
+    return launch_hops(hops, count, fmt, reinterpret_cast<cudaStream_t>(stream), false, flags);
 }
 
 extern "C" fp8q_status_t fp8q_ring_hop_bf16_requant(const uint8_t* in_codes, const float* in_scales,

@@ -19,6 +19,8 @@ namespace fp8q {
 // order like their bit patterns).
 __global__ void __launch_bounds__(256)
 tensor_amax_kernel(const uint16_t* __restrict__ x, size_t n, float* scale_amax) {
+    dependency_wait();
+    allow_dependents();
     uint32_t m = 0;
     const size_t n8 = n / 8;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -38,6 +40,8 @@ tensor_amax_kernel(const uint16_t* __restrict__ x, size_t n, float* scale_amax) 
 template <int FMT>
 __global__ void __launch_bounds__(256)
 tensor_encode_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __restrict__ codes, float* scale_amax) {
+    dependency_wait();
+    allow_dependents();
     const float amax = scale_amax[1];
     const float s = block_scale<FMT>(amax);
     const size_t n8 = n / 8;
@@ -66,11 +70,9 @@ static fp8q_status_t launch_tensorwise(const uint16_t* x, size_t n, uint8_t* cod
     static int r1 = resident_blocks(tensor_amax_kernel, 256);
     static int r2 = resident_blocks(tensor_encode_kernel<FMT>, 256);
     const size_t units = (n + 7) / 8;
-    tensor_amax_kernel<<<grid_for((units + 255) / 256, r1), 256, 0, s>>>(x, n, scale_amax);
-    fp8q_status_t st = launch_status();
+    const fp8q_status_t st = launch(tensor_amax_kernel, grid_for((units + 255) / 256, r1), 256, 0, s, x, n, scale_amax);
     if (st != FP8Q_OK) return st;
-    tensor_encode_kernel<FMT><<<grid_for((units + 255) / 256, r2), 256, 0, s>>>(x, n, codes, scale_amax);
-    return launch_status();
+    return launch(tensor_encode_kernel<FMT>, grid_for((units + 255) / 256, r2), 256, 0, s, x, n, codes, scale_amax);
 }
 
 }  // namespace fp8q
