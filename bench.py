@@ -542,47 +542,80 @@ def _oracle_inputs():
     return _ORACLE_INPUTS
 
 
-def oracle_sample(fraction):
-    """The oracle on a contiguous fraction of the same workload (rank 0's
-    data): returns (algorithmic bytes, elements, seconds, description)."""
-    import oracle as orc
-    inp = _oracle_inputs()
-    k = len(inp["shards"])
-    n_full = inp["shards"][0].size
-    n = max(128, int(n_full * fraction) // 128 * 128)
-    shards = [sh[:n].copy() for sh in inp["shards"]]
-    mats = []
-    for x, b, m, kk in inp["mats"]:
-        if b > 1:
-            bs = max(1, int(round(b * fraction)))
-            mats.append((x[:bs].copy(), bs, m, kk))
-        else:
-            ms = max(128, int(m * fraction) // 128 * 128)
-            mats.append((x[0, :ms].copy(), 1, ms, kk))
+def _oracle_step(orc, shards, mats):
+    """One step of the oracle on the given slices of the bucket shards and
+    the layer tensors: returns (algorithmic bytes, elements)."""
+    k = len(shards)
+    n = shards[0].size
     nbytes = elems = 0
-    t0 = time.perf_counter()
-    q = {}
-    for f in (0, 1):
-        q[f] = [orc.quantize_blockwise(sh, f) for sh in shards]
-        nbytes += bytes_quantize(k * n)
-        elems += k * n
-    for f in (0, 1):
-        orc.dequant_reduce([c for c, _ in q[f]], [s for _, s in q[f]], f)
-        nbytes += bytes_reduce(n, k)
-        elems += n
-    c, s = q[0][0]
-    for h in range(1, k):
-        c, s, _ = orc.ring_hop(c, s, shards[h], 0)
-        nbytes += bytes_hop(n, h == k - 1)
-        elems += n
+    if n:
+        q = {}
+        for f in (0, 1):
+            q[f] = [orc.quantize_blockwise(sh, f) for sh in shards]
+            nbytes += bytes_quantize(k * n)
+            elems += k * n
+        for f in (0, 1):
+            orc.dequant_reduce([c for c, _ in q[f]], [s for _, s in q[f]], f)
+            nbytes += bytes_reduce(n, k)
+            elems += n
+        c, s = q[0][0]
+        for h in range(1, k):
+            c, s, _ = orc.ring_hop(c, s, shards[h], 0)
+            nbytes += bytes_hop(n, h == k - 1)
+            elems += n
     for x, b, m, kk in mats:
+        if b * m == 0:
+            continue
         orc.mxfp8_quantize_swizzled(x, b, m, kk)
         nbytes += bytes_mxfp8(b, m, kk, orc.swizzled_scale_bytes(b, m, kk))
         elems += b * m * kk
+    return nbytes, elems
+
+
+def oracle_sample(fraction, threads=1):
+    """The oracle on a contiguous fraction of the same workload (rank 0's
+    data): returns (algorithmic bytes, elements, seconds, description).  With
+    threads > 1 the sample is cut into that many disjoint, 128-aligned parts
+    (bucket elements, experts, attention rows) run at once; the oracle's
+    calls release the interpreter lock, so the threads run in parallel."""
+    import concurrent.futures as cf
+    import oracle as orc
+    inp = _oracle_inputs()
+    n_full = inp["shards"][0].size
+    n = max(128, int(n_full * fraction) // 128 * 128)
+    mats_all = []
+    for x, b, m, kk in inp["mats"]:
+        if b > 1:
+            mats_all.append((x, max(1, int(round(b * fraction))), m, kk, True))
+        else:
+            mats_all.append((x, 1, max(128, int(m * fraction) // 128 * 128), kk, False))
+
+    def part(i, t):
+        lo, hi = (n // 128) * i // t * 128, (n // 128) * (i + 1) // t * 128
+        shards = [sh[lo:hi].copy() for sh in inp["shards"]]
+        mats = []
+        for x, b, m, kk, batched in mats_all:
+            if batched:
+                b0, b1 = b * i // t, b * (i + 1) // t
+                mats.append((x[b0:b1].copy(), b1 - b0, m, kk))
+            else:
+                r0, r1 = (m // 128) * i // t * 128, (m // 128) * (i + 1) // t * 128
+                mats.append((x[0, r0:r1].copy(), 1, r1 - r0, kk))
+        return shards, mats
+
+    parts = [part(i, threads) for i in range(threads)]
+    t0 = time.perf_counter()
+    if threads == 1:
+        res = [_oracle_step(orc, *parts[0])]
+    else:
+        with cf.ThreadPoolExecutor(threads) as ex:
+            res = list(ex.map(lambda p_: _oracle_step(orc, *p_), parts))
     dt = time.perf_counter() - t0
+    nbytes = sum(r[0] for r in res)
+    elems = sum(r[1] for r in res)
     desc = (f"{fraction:.4g} of one step: the first {n} elements of each of the 8 bucket shards (both formats, "
             f"reduce, 7 hops) and the first {fraction:.4g} of the experts / rows of each layer tensor; "
-            f"single-threaded oracle")
+            + ("single-threaded oracle" if threads == 1 else f"cut into {threads} disjoint parts on {threads} threads"))
     return nbytes, elems, dt, desc
 
 
@@ -813,6 +846,121 @@ def extra_rows(wl, torch, peak):
     return out
 
 
+def vec3p5b_row(wl, torch, peak, reps=3):
+    """The 3.5e9-element gradient vector: 4 shards quantized to e4m3 (one
+    launch per shard), then the 4-shard fused reduce to bf16 streamed in
+    2^27-element chunks (launched back to back).  The inputs are drawn on the
+    device from a seeded Philox normal with the vector's distribution
+    (N(0, 1e-4^2), 1e-4 outliers x1000, the same 64 zero blocks per shard);
+    the full-size parity test uses the counter-based generator instead, which
+    is too slow on the host for a timing row.  Medians of `reps`."""
+    import gen
+    w, dev, st = wl.w, wl.dev, wl.stream
+    L = w.lib()
+    n, k, chunk = gen.VEC_N, gen.VEC_K, gen.VEC_CHUNK
+    nb = nscales(n)
+    free, _ = torch.cuda.mem_get_info(dev)
+    need = k * (n + 4 * nb) + 2 * 2 * n
+    if free < need * 1.1:
+        return {"skipped": f"needs {need / 2**30:.1f} GiB, {free / 2**30:.1f} GiB free"}
+    x = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    codes = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(k)]
+    scales = [torch.empty(nb, dtype=torch.float32, device=dev) for _ in range(k)]
+    out = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    vp = ctypes.c_void_p
+    sp_ = vp(st.cuda_stream)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+    q_ms = []
+    for r in range(k):
+        g = torch.Generator(device=dev)
+        g.manual_seed(100 + r)
+        for c0 in range(0, n, chunk):
+            cnt = min(chunk, n - c0)
+            v = torch.randn(cnt, device=dev, generator=g).mul_(1e-4)
+            hit = torch.rand(cnt, device=dev, generator=g) < 1e-4
+            v[hit] *= 1000.0
+            x[c0:c0 + cnt].copy_(v)
+            del v, hit
+        zb = torch.from_numpy(gen.vec_zero_blocks(r).astype("int64")).to(dev)
+        idx = (zb[:, None] * 128 + torch.arange(128, device=dev)[None, :]).reshape(-1)
+        x[idx[idx < n]] = 0
+        args = (vp(x.data_ptr()), ctypes.c_size_t(n), ctypes.c_int(0), vp(codes[r].data_ptr()),
+                vp(scales[r].data_ptr()), sp_)
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            a, b = ev(), ev()
+            a.record(st)
+            if L.fp8q_quantize_blockwise(*args) != 0:
+                raise RuntimeError("3.5B quantize failed")
+            b.record(st)
+            torch.cuda.synchronize()
+            q_ms.append(a.elapsed_time(b))
+    del x
+    calls = []
+    for c0 in range(0, n, chunk):
+        cnt = min(chunk, n - c0)
+        b0 = c0 // 128
+        cp = (vp * k)(*[codes[r].data_ptr() + c0 for r in range(k)])
+        spp = (vp * k)(*[scales[r].data_ptr() + 4 * b0 for r in range(k)])
+        calls.append((cp, spp, ctypes.c_int(k), ctypes.c_size_t(cnt), ctypes.c_int(0), vp(out.data_ptr() + 2 * c0),
+                      vp(None), sp_))
+    r_ms = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record(st)
+        for c in calls:
+            if L.fp8q_dequant_reduce(*c) != 0:
+                raise RuntimeError("3.5B reduce failed")
+        b.record(st)
+        torch.cuda.synchronize()
+        r_ms.append(a.elapsed_time(b))
+    del codes, scales, out
+    torch.cuda.empty_cache()
+    q_med = sorted(q_ms)[len(q_ms) // 2]
+    r_med = sorted(r_ms)[len(r_ms) // 2]
+    qb = bytes_quantize(n)
+    rb = k * (n + 4 * nb) + 2 * n
+    return {"elements": n, "shards": k,
+            "quantize": {"launches": k * reps, "ms_median": round(q_med, 3), "bytes": qb,
+                         "GB/s": round(qb / (q_med * 1e-3) / 1e9, 1),
+                         "frac_of_peak": round(qb / (q_med * 1e-3) / 1e9 / peak, 4)},
+            "reduce_streamed": {"chunks": len(calls), "ms_median": round(r_med, 3), "bytes": rb,
+                                "GB/s": round(rb / (r_med * 1e-3) / 1e9, 1),
+                                "frac_of_peak": round(rb / (r_med * 1e-3) / 1e9 / peak, 4)},
+            "inputs": "device Philox normal, seeds 100 + shard, with the vector's outliers and zero blocks"}
+
+
+def host_cpu():
+    """The host cores the oracle runs on."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "processor name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:                 # Arm: implementer and part numbers
+        ids = {}
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    key = line.split(":")[0].strip()
+                    if key in ("CPU implementer", "CPU part") and key not in ids:
+                        ids[key] = line.split(":", 1)[1].strip()
+        except OSError:
+            pass
+        if ids:
+            model = " ".join(f"{k_} {v_}" for k_, v_ in ids.items())
+    return {"nproc": os.cpu_count(), "usable": len(os.sched_getaffinity(0)), "model": model,
+            "arch": os.uname().machine}
+
+
 # ---------------------------------------------------------------- main ----
 def main():
     ap = argparse.ArgumentParser()
@@ -822,6 +970,7 @@ def main():
     ap.add_argument("--impl", default="fp8q", choices=["fp8q", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-vec3p5b", action="store_true", help="skip the 3.5e9-element vector row")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
                     help="launch one kernel of the step a few times on its bench inputs and exit (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=3)
@@ -879,11 +1028,12 @@ def main():
     for i in range(nbreak):
         for j, (kind, nbytes, elems, _, _) in enumerate(wl.launches):
             dt = break_ev[i][2 * j].elapsed_time(break_ev[i][2 * j + 1])
-            d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "bytes": 0, "elems": 0})
+            d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "bytes": 0, "elems": 0, "all": []})
             d["launches"] += 1
             d["ms"] += dt
             d["bytes"] += nbytes
             d["elems"] += elems
+            d["all"].append(dt)
     dom = max(per_kind, key=lambda k: per_kind[k]["ms"])
 
     # each run of launches of one kernel timed as a whole: inside a run the
@@ -960,12 +1110,16 @@ def main():
 
     peak, peak_kind = measured_peaks()
     extras = extra_rows(wl, torch, peak)
+    if not args.no_vec3p5b:
+        extras["vec3p5b"] = vec3p5b_row(wl, torch, peak)
     total_ms = sum(d["ms"] for d in per_kind.values())
     kernels = {}
     for kind, d in per_kind.items():
         avg_ms = d["ms"] / d["launches"]
         gbs = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+        med_ms = sorted(d["all"])[len(d["all"]) // 2]
         kernels[kind] = {"launches_per_step": d["launches"] // nbreak, "avg_us": round(1e3 * avg_ms, 2),
+                         "median_us": round(1e3 * med_ms, 2),
                          "bytes_per_launch": d["bytes"] // d["launches"], "GB/s": round(gbs, 1),
                          "frac_of_peak": round(gbs / peak, 4), "share": round(d["ms"] / total_ms, 4)}
     achieved = dom_bytes * dom_launches / (dom_ms * 1e-3) / 1e9
@@ -1008,7 +1162,16 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         nbytes, elems, dt, desc = oracle_sample(oracle_fraction_for(10.0))
         line["cpu_baseline"] = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": desc, "seconds": round(dt, 2)}
+                                "sample": desc, "seconds": round(dt, 2), "host": host_cpu()}
+        ncores = len(os.sched_getaffinity(0))
+        if ncores > 1:
+            # the same oracle over independent parts on every usable core, a
+            # second baseline row; its sample is sized for about 5 s
+            frac = min(1.0, oracle_fraction_for(5.0) * ncores)
+            nb_all, _, dt_all, desc_all = oracle_sample(frac, threads=ncores)
+            line["cpu_baseline_all_cores"] = {"value": round(nb_all / dt_all / 1e9, 4), "unit": "GB/s",
+                                              "cores": ncores, "kind": "oracle", "sample": desc_all,
+                                              "seconds": round(dt_all, 2)}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
