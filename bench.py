@@ -743,22 +743,32 @@ def fused_vs_naive(wl, torch, reps=20):
     return out
 
 
-def ring_sweep(wl, torch, payloads=(64 << 20, 256 << 20), reps=10):
-    """One ring hop (e4m3, with the bf16 output of the last hop) at large
-    per-hop payloads, outside the step: the size range the >= 70%-of-peak
-    bar is stated for."""
+def ring_sweep(wl, torch, payloads=(64 << 20, 128 << 20, 256 << 20), reps=10):
+    """The ring at large per-hop payloads, outside the step: the size range
+    the >= 70%-of-peak bar is stated for.  Per payload: one hop (e4m3, with
+    the bf16 output of a last hop) timed alone, and the 7-hop chain of a ring
+    of 8 launched back to back as the step launches it (each hop's local
+    partial copied early).  Partials 0 and 1 come from the counter-based
+    generator; 2..7 from a seeded device-side draw of the same
+    distribution, N(0, 1e-3^2)."""
     import gen
     L = wl.L
+    w = wl.w
     vp = ctypes.c_void_p
     s = vp(wl.stream.cuda_stream)
     flush = L2Flush(torch, wl.dev)
     out = {}
+    P = gen.RING_PARTIALS
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
     for payload in payloads:
         n = payload // 2
+        nb = nscales(n)
         x0 = gen.ring_partial(0, n).to(wl.dev)
         x1 = gen.ring_partial(1, n).to(wl.dev)
         c0 = torch.empty(n, dtype=torch.uint8, device=wl.dev)
-        s0 = torch.empty(nscales(n), dtype=torch.float32, device=wl.dev)
+        s0 = torch.empty(nb, dtype=torch.float32, device=wl.dev)
         c1 = torch.empty_like(c0)
         s1 = torch.empty_like(s0)
         ob = torch.empty(n, dtype=torch.bfloat16, device=wl.dev)
@@ -771,7 +781,7 @@ def ring_sweep(wl, torch, payloads=(64 << 20, 256 << 20), reps=10):
         tot = 0.0
         for _ in range(reps):
             flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a, b = ev(), ev()
             a.record(wl.stream)
             if L.fp8q_ring_hop(*args) != 0:
                 raise RuntimeError("ring sweep hop failed")
@@ -780,8 +790,40 @@ def ring_sweep(wl, torch, payloads=(64 << 20, 256 << 20), reps=10):
             tot += a.elapsed_time(b)
         us = 1e3 * tot / reps
         nbytes = bytes_hop(n, True)
-        out[f"{payload >> 20}MiB"] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1)}
-        del x0, x1, c0, s0, c1, s1, ob
+        row = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1)}
+        # the 7-hop chain
+        g = torch.Generator(device=wl.dev)
+        g.manual_seed(200 + payload)
+        parts = [x0, x1] + [torch.randn(n, device=wl.dev, generator=g).mul_(1e-3).to(torch.bfloat16)
+                            for _ in range(P - 2)]
+        outs = [(torch.empty(n, dtype=torch.uint8, device=wl.dev), torch.empty(nb, dtype=torch.float32, device=wl.dev))
+                for _ in range(P - 1)]
+        hops = []
+        prev = (c0, s0)
+        for h in range(1, P):
+            oc, os_ = outs[h - 1]
+            hops.append((w.fp8q_hop_t * 1)(w.fp8q_hop_t(prev[0].data_ptr(), prev[1].data_ptr(), parts[h].data_ptr(), n,
+                                                         oc.data_ptr(), os_.data_ptr(),
+                                                         ob.data_ptr() if h == P - 1 else None)))
+            prev = (oc, os_)
+        ready = ctypes.c_uint(w.FP8Q_HOP_LOCAL_READY)
+        times = []
+        for i in range(reps + 2):
+            flush()
+            a, b = ev(), ev()
+            a.record(wl.stream)
+            for hp in hops:
+                if L.fp8q_ring_hop_group_ex(hp, 1, 0, ready, s) != 0:
+                    raise RuntimeError("ring sweep chain failed")
+            b.record(wl.stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                times.append(a.elapsed_time(b))
+        cms = sorted(times)[len(times) // 2]
+        cbytes = (P - 2) * bytes_hop(n, False) + bytes_hop(n, True)
+        row["chain_7_hops"] = {"us": round(1e3 * cms, 2), "bytes": cbytes, "GB/s": round(cbytes / (cms * 1e-3) / 1e9, 1)}
+        out[f"{payload >> 20}MiB"] = row
+        del x0, x1, c0, s0, c1, s1, ob, parts, outs, hops
     return out
 
 
@@ -1155,7 +1197,10 @@ def main():
         "gpu_launches": nl * steps,
         "fused_vs_naive_reduce": fvn,
         "next_rows": extras,
-        "ring_hop_sweep": {k: dict(v, frac_of_peak=round(v["GB/s"] / peak, 4)) for k, v in sweep.items()},
+        "ring_hop_sweep": {k: dict(v, frac_of_peak=round(v["GB/s"] / peak, 4),
+                                   chain_7_hops=dict(v["chain_7_hops"],
+                                                     frac_of_peak=round(v["chain_7_hops"]["GB/s"] / peak, 4)))
+                           for k, v in sweep.items()},
         "clocks": clock_info,
         "cpu_baseline": None,
     }
