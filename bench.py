@@ -975,6 +975,30 @@ def vec3p5b_row(wl, torch, peak, reps=3):
             "inputs": "device Philox normal, seeds 100 + shard, with the vector's outliers and zero blocks"}
 
 
+def hbm_copy_check(torch, dev, nbytes=2 << 30, reps=5):
+    """A device-to-device copy of `nbytes` on this GPU in the same run (read
+    plus written bytes over the median time): the box's own copy rate, shown
+    next to the peak that the fractions use."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    dst.copy_(src)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = sorted(times)[len(times) // 2]
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"GB/s": round(2 * nbytes / (ms * 1e-3) / 1e9, 1), "bytes_moved": 2 * nbytes, "ms_median": round(ms, 4),
+            "what": "device-to-device copy of 2 GiB, median of 5"}
+
+
 def host_cpu():
     """The host cores the oracle runs on."""
     model = None
@@ -1151,6 +1175,7 @@ def main():
         return
 
     peak, peak_kind = measured_peaks()
+    copy_check = hbm_copy_check(torch, dev)
     extras = extra_rows(wl, torch, peak)
     if not args.no_vec3p5b:
         extras["vec3p5b"] = vec3p5b_row(wl, torch, peak)
@@ -1180,6 +1205,7 @@ def main():
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "avg_us": round(1e3 * dom_ms / dom_launches, 2),
+                     "copy_check": copy_check,
                      "timing": "events around each launch of this kernel in the K timed steps"},
         "kernels": kernels,
         "kernels_timing": f"separate pass of {nbreak} steps with events around every launch",

@@ -17,14 +17,23 @@ fp8q_status_t cuda_status(cudaError_t e) {
     return FP8Q_ERR_CUDA;
 }
 
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
 int sm_count() {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    static std::atomic<int> cached[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    if (dev < kMaxDevices) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
-    if (dev < 64) cached[dev] = n;
+    if (dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

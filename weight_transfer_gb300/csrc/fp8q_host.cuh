@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "fp8q.h"
@@ -36,15 +37,49 @@ unsigned unit_errors_reduce(bool clear);
 unsigned unit_errors_ring_hop(bool clear);
 unsigned unit_errors_mxfp8(bool clear);
 
+// Devices whose per-device state is cached; others are set up on every call.
+constexpr int kMaxDevices = 64;
+
+// The calling thread's current device, or -1.
+int current_device();
+
 // SM count of the current device (cached per device).
 int sm_count();
 
-// Blocks of `threads` threads of `kernel` that fit on one SM (cached by the caller).
+// Blocks of `threads` threads of `kernel` that fit on one SM.
 template <class K>
 int resident_blocks(K kernel, int threads, size_t smem = 0) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
     return n;
+}
+
+// One-time preparation of a kernel on each device: the opt-in to more than
+// 48 KB of dynamic shared memory (a function attribute that applies to the
+// device current when it is set) and the kernel's resident blocks per SM.
+// Cached per device, so that one process may drive several GPUs; concurrent
+// first calls repeat the same idempotent work.  A cache object must have
+// static storage duration (its counters start at zero).
+struct KernelCache {
+    std::atomic<int> resident[kMaxDevices];
+};
+
+template <class K>
+fp8q_status_t prepare_kernel(KernelCache& kc, K kernel, int threads, size_t smem, size_t smem_optin, int* resident) {
+    const int dev = current_device();
+    const bool cached = dev >= 0 && dev < kMaxDevices;
+    int r = cached ? kc.resident[dev].load(std::memory_order_acquire) : 0;
+    if (r == 0) {
+        if (smem_optin > 0) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_optin);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        r = resident_blocks(kernel, threads, smem);
+        if (cached) kc.resident[dev].store(r, std::memory_order_release);
+    }
+    *resident = r;
+    return FP8Q_OK;
 }
 
 // Persistent grid: enough blocks to fill every SM `resident` deep, but never

@@ -286,10 +286,10 @@ static fp8q_status_t launch_group(const mxfp8_tensor_t* tensors, int count, cuda
     if (used == 0) return FP8Q_OK;
     g.tile_start[used] = start;
     g.count = used;
-    static const cudaError_t attr =
-        cudaFuncSetAttribute(mxfp8_quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMxSmem);
-    if (attr != cudaSuccess) return cuda_status(attr);
-    static int resident = resident_blocks(mxfp8_quantize_kernel, kMxThreads, kMxSmem);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc, mxfp8_quantize_kernel, kMxThreads, kMxSmem, kMxSmem, &resident);
+    if (st != FP8Q_OK) return st;
     const unsigned grid = grid_for((size_t)start, resident);
     return launch(mxfp8_quantize_kernel, grid, kMxThreads, kMxSmem, stream, g);
 }

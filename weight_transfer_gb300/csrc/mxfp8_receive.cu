@@ -108,7 +108,10 @@ extern "C" fp8q_status_t mxfp8_dequantize_swizzled(const uint8_t* codes, const u
     if (!aligned16(codes) || !aligned16(scales_swizzled) || !aligned16(out_bf16)) return FP8Q_ERR_ALIGN;
     const size_t sb = mxfp8_swizzled_scale_bytes(batch, m, k);
     if (overlaps(out_bf16, 2 * n, codes, n) || overlaps(out_bf16, 2 * n, scales_swizzled, sb)) return FP8Q_ERR_ALIAS;
-    static int resident = resident_blocks(mxfp8_dequantize_kernel, 256);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t pst = prepare_kernel(kc, mxfp8_dequantize_kernel, 256, 0, 0, &resident);
+    if (pst != FP8Q_OK) return pst;
     const size_t units = n / 16;
     return launch(mxfp8_dequantize_kernel, grid_for((units + 255) / 256, resident), 256, 0,
                   reinterpret_cast<cudaStream_t>(stream), codes, scales_swizzled, m, k, units,
@@ -125,7 +128,10 @@ extern "C" fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, 
     if (!aligned16(scales_swizzled) || !aligned16(scales_rowmajor)) return FP8Q_ERR_ALIGN;
     if (overlaps(scales_rowmajor, total, scales_swizzled, mxfp8_swizzled_scale_bytes(batch, m, k)))
         return FP8Q_ERR_ALIAS;
-    static int resident = resident_blocks(mxfp8_unswizzle_kernel, 256);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t pst = prepare_kernel(kc, mxfp8_unswizzle_kernel, 256, 0, 0, &resident);
+    if (pst != FP8Q_OK) return pst;
     return launch(mxfp8_unswizzle_kernel, grid_for((total + 255) / 256, resident), 256, 0,
                   reinterpret_cast<cudaStream_t>(stream), scales_swizzled, m, (int64_t)(k / MXFP8_BLOCK), total,
                   scales_rowmajor);
@@ -138,7 +144,10 @@ extern "C" fp8q_status_t fp8q_count_mismatches(const void* a, const void* b, siz
     if (!a || !b || !count) return FP8Q_ERR_NULL;
     if (!aligned16(a) || !aligned16(b) || (reinterpret_cast<uintptr_t>(count) & 7u)) return FP8Q_ERR_ALIGN;
     if (overlaps(count, 8, a, nbytes) || overlaps(count, 8, b, nbytes)) return FP8Q_ERR_ALIAS;
-    static int resident = resident_blocks(count_mismatches_kernel, 256);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t pst = prepare_kernel(kc, count_mismatches_kernel, 256, 0, 0, &resident);
+    if (pst != FP8Q_OK) return pst;
     return launch(count_mismatches_kernel, grid_for((nbytes / 16 + 255) / 256 + 1, resident), 256, 0,
                   reinterpret_cast<cudaStream_t>(stream), static_cast<const uint8_t*>(a),
                   static_cast<const uint8_t*>(b), nbytes, count);

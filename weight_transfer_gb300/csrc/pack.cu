@@ -121,7 +121,10 @@ extern "C" fp8q_status_t fp8q_copy_segments(const fp8q_copy_t* segs, int count, 
     if (used == 0) return FP8Q_OK;
     tab.piece_start[used] = pieces;
     tab.count = used;
-    static int resident = resident_blocks(copy_segments_kernel, 256);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t pst = prepare_kernel(kc, copy_segments_kernel, 256, 0, 0, &resident);
+    if (pst != FP8Q_OK) return pst;
     return launch(copy_segments_kernel, grid_for((size_t)pieces, resident), 256, 0,
                   reinterpret_cast<cudaStream_t>(stream), tab);
 }

@@ -161,10 +161,11 @@ encode_f32_kernel(const float* __restrict__ x, size_t n, uint8_t* __restrict__ c
 template <int FMT>
 static fp8q_status_t launch_quantize(const uint16_t* x, size_t n, uint8_t* codes, float* scales,
                                      cudaStream_t stream) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        quantize_blockwise_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQuantSmem);
-    if (attr != cudaSuccess) return cuda_status(attr);
-    static int resident = resident_blocks(quantize_blockwise_kernel<FMT>, kQuantThreads, kQuantSmem);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc, quantize_blockwise_kernel<FMT>, kQuantThreads, kQuantSmem,
+                                            kQuantSmem, &resident);
+    if (st != FP8Q_OK) return st;
     const size_t tiles = (n + kQuantTile - 1) / kQuantTile;
     const unsigned grid = grid_for(tiles, resident);
     return launch(quantize_blockwise_kernel<FMT>, grid, kQuantThreads, kQuantSmem, stream, x, n, codes, scales);
@@ -172,7 +173,10 @@ static fp8q_status_t launch_quantize(const uint16_t* x, size_t n, uint8_t* codes
 
 template <int FMT>
 static fp8q_status_t launch_encode(const float* x, size_t n, uint8_t* codes, cudaStream_t stream) {
-    static int resident = resident_blocks(encode_f32_kernel<FMT>, 256);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc, encode_f32_kernel<FMT>, 256, 0, 0, &resident);
+    if (st != FP8Q_OK) return st;
     const size_t units = (n + 3) / 4;
     const unsigned grid = grid_for((units + 255) / 256, resident * 2);
     return launch(encode_f32_kernel<FMT>, grid, 256, 0, stream, x, n, codes);

@@ -235,18 +235,14 @@ sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, size_t slot, uint1
 template <int FMT, bool B, bool F, bool SUM, int KMAX>
 static fp8q_status_t launch_reduce_k(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
     auto kernel = dequant_reduce_kernel<FMT, B, F, SUM, KMAX>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [&] {
-        attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)red_smem_bytes(KMAX));
-    });
-    if (attr_err != cudaSuccess) return cuda_status(attr_err);
-    static int resident[KMAX + 1] = {0};      // per k; benign race on first fill
+    // one cache per shard count: the stage size, and so the occupancy, depends on k
+    static KernelCache kc[KMAX + 1];
     const size_t smem = red_smem_bytes(k);
-    if (resident[k] == 0) resident[k] = resident_blocks(kernel, kRedThreads, smem);
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc[k], kernel, kRedThreads, smem, red_smem_bytes(KMAX), &resident);
+    if (st != FP8Q_OK) return st;
     const size_t tiles = (n + kRedTile - 1) / kRedTile;
-    const unsigned grid = grid_for(tiles, resident[k]);
+    const unsigned grid = grid_for(tiles, resident);
     return launch(kernel, grid, kRedThreads, smem, s, sh, k, n, ob, of);
 }
 
@@ -272,7 +268,10 @@ static fp8q_status_t launch_reduce(const ShardPtrs& sh, int k, size_t n, uint16_
 template <bool B, bool F>
 static fp8q_status_t launch_sum_t(const float* ws, int k, size_t n, size_t stride, uint16_t* ob, float* of,
                                   cudaStream_t s) {
-    static int resident = resident_blocks(sum_f32_kernel<B, F>, kRedThreads);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc, sum_f32_kernel<B, F>, kRedThreads, 0, 0, &resident);
+    if (st != FP8Q_OK) return st;
     const size_t units = (n + 15) / 16;
     const unsigned grid = grid_for((units + kRedThreads - 1) / kRedThreads, resident);
     return launch(sum_f32_kernel<B, F>, grid, kRedThreads, 0, s, ws, k, n, stride, ob, of);
@@ -379,7 +378,6 @@ namespace fp8q {
 
 static __device__ __align__(256) float g_static_scratch[FP8Q_STATIC_SCRATCH_FLOATS];
 
-constexpr int kMaxDevices = 64;
 static std::mutex g_static_scratch_mu;
 static float* g_static_scratch_ptr[kMaxDevices];
 

@@ -264,10 +264,10 @@ static void hop_ranges(const fp8q_hop_t& hp, const void* p[6], size_t sz[6]) {
 
 template <int FMT, bool REQ>
 static fp8q_status_t launch_hop_kernel(const HopGroup& g, size_t tiles, cudaStream_t stream) {
-    static const cudaError_t attr = cudaFuncSetAttribute(ring_hop_kernel<FMT, REQ>,
-                                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHopSmem);
-    if (attr != cudaSuccess) return cuda_status(attr);
-    static int resident = resident_blocks(ring_hop_kernel<FMT, REQ>, kHopThreads, kHopSmem);
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc, ring_hop_kernel<FMT, REQ>, kHopThreads, kHopSmem, kHopSmem, &resident);
+    if (st != FP8Q_OK) return st;
     return launch(ring_hop_kernel<FMT, REQ>, grid_for(tiles, resident), kHopThreads, kHopSmem, stream, g);
 }
 

@@ -67,8 +67,11 @@ static fp8q_status_t launch_tensorwise(const uint16_t* x, size_t n, uint8_t* cod
                                        cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(scale_amax + 1, 0, sizeof(float), s);
     if (e != cudaSuccess) return cuda_status(e);
-    static int r1 = resident_blocks(tensor_amax_kernel, 256);
-    static int r2 = resident_blocks(tensor_encode_kernel<FMT>, 256);
+    static KernelCache kc1, kc2;
+    int r1 = 0, r2 = 0;
+    fp8q_status_t pst = prepare_kernel(kc1, tensor_amax_kernel, 256, 0, 0, &r1);
+    if (pst == FP8Q_OK) pst = prepare_kernel(kc2, tensor_encode_kernel<FMT>, 256, 0, 0, &r2);
+    if (pst != FP8Q_OK) return pst;
     const size_t units = (n + 7) / 8;
     const fp8q_status_t st = launch(tensor_amax_kernel, grid_for((units + 255) / 256, r1), 256, 0, s, x, n, scale_amax);
     if (st != FP8Q_OK) return st;
