@@ -127,3 +127,32 @@ def test_hop_chain_local_ready(w, orc, fmt, n):
             assert_same_f32(hops[h - 1][1], s, f"flags {flags} hop {h} scales")
     for flags, (_, b) in res.items():
         assert_same(b, eb, f"flags {flags} final bf16")
+
+
+def test_ddp_ring_chain_as_the_bench_launches_it(w, orc):
+    # full size: the 8 DDP shards in one [8, n] allocation, hop 0 = the e4m3
+    # quantize of shard 0 (part of the one-launch bucket quantize), hops 1..7
+    # grouped calls of one with the early local copy, launched back to back,
+    # the last with the bf16 output; every hop checked element by element
+    n, k = gen.DDP_N, gen.DDP_K
+    host = [gen.ddp_shard(r) for r in range(k)]
+    bucket = torch.empty((k, n), dtype=torch.bfloat16, device="cuda")
+    for r in range(k):
+        bucket[r].copy_(host[r])
+    qc, qs = w.fp8q_quantize_blockwise(bucket.view(-1), 0)
+    prev = (qc[:n], qs[:n // 128])
+    outs = []
+    last = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    for h in range(1, k):
+        hp = {"in_codes": prev[0], "in_scales": prev[1], "local": bucket[h],
+              "out_bf16": last if h == k - 1 else None}
+        (c, s, _), = w.fp8q_ring_hop_group_ex([hp], 0, w.FP8Q_HOP_LOCAL_READY)
+        outs.append((c, s))
+        prev = (c, s)
+    got = [(u8(c), s.cpu().numpy()) for c, s in outs]
+    c, s = orc.quantize_blockwise(bits16(host[0]), 0)
+    for h in range(1, k):
+        c, s, eb = orc.ring_hop(c, s, bits16(host[h]), 0)
+        assert_same(got[h - 1][0], c, f"hop {h} codes")
+        assert_same_f32(got[h - 1][1], s, f"hop {h} scales")
+    assert_same(bits16(last), eb, "final bf16")

@@ -76,11 +76,17 @@ def test_quantize_ddp_bucket_config(w, orc, fmt):
         return orc.quantize_blockwise(bits16(gen.ddp_shard(r)), fmt)
     with cf.ThreadPoolExecutor(8) as ex:
         expected = list(ex.map(oracle, range(gen.DDP_K)))
-    for r in range(gen.DDP_K):
-        x = gen.ddp_shard(r).cuda()
-        c, s = w.fp8q_quantize_blockwise(x, fmt)
-        assert_same_f32(s.cpu().numpy(), expected[r][1], f"scales shard {r}")
-        assert_same(u8(c), expected[r][0], f"codes shard {r}")
+    # one launch over the [8, n] bucket, as the bench quantizes it (n is a
+    # multiple of 128, so no block straddles two shards)
+    n, k = gen.DDP_N, gen.DDP_K
+    bucket = torch.empty((k, n), dtype=torch.bfloat16, device="cuda")
+    for r in range(k):
+        bucket[r].copy_(gen.ddp_shard(r))
+    c, s = w.fp8q_quantize_blockwise(bucket.view(-1), fmt)
+    c, s = u8(c).reshape(k, n), s.cpu().numpy().reshape(k, n // 128)
+    for r in range(k):
+        assert_same_f32(s[r], expected[r][1], f"scales shard {r}")
+        assert_same(c[r], expected[r][0], f"codes shard {r}")
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
