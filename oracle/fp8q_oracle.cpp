@@ -27,7 +27,7 @@
 //       X = floor(log2(amax)) - emax_elem.
 //
 // The pages print no formula or code for any of these steps.  The readings
-// taken where they are silent are (numbered as in the design notes):
+// taken where they are silent are these (numbered O1..O17):
 //  O1 block of 128 elements with one fp32 scale (the only reading that gives
 //     P1's 48.4% byte saving exactly);
 //  O2/O3 s = RN(amax / Fmax); code = RNE_fp8(RN_fp32(x / s)), a true IEEE
@@ -42,7 +42,9 @@
 //  O11/O12 E8M0 e = clamp(floor(log2 amax) - 8 + 127, 0, 254), amax == 0
 //     gives e = 0;
 //  O14 scale swizzle: 128x4 tiles of 512 bytes,
-//     (r%32)*16 + ((r%128)/32)*4 + (j%4) inside a tile.
+//     (r%32)*16 + ((r%128)/32)*4 + (j%4) inside a tile.  The formula is
+//     pinned by a hand table and a bijection check, but the choice of this
+//     layout is parity unpinned: nothing on the pages fixes it.
 //  O17 K % 32 != 0 is rejected; K == 32 keeps its one real scale column.
 
 #include <cmath>
