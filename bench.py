@@ -523,6 +523,11 @@ class Workload:
         self.sets[0].run()
         self.launches = self.sets[0].launches
         torch.cuda.synchronize(self.dev)
+        # the pipelined run's last results, read back to the host, against a
+        # device-resident run on the same inputs: byte for byte
+        self.e2e_outputs_equal = all(
+            torch.equal(h.contiguous().view(-1).view(torch.uint8), d.contiguous().view(-1).cpu().view(torch.uint8))
+            for h, d in zip(self.h_out, self.sets[0].outputs))
         return start.elapsed_time(end) / steps, bi, bo
 
 
@@ -1217,6 +1222,7 @@ def main():
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
                 "copy_GBps_alone": getattr(wl, "copy_gbps", None),
+                "outputs_equal_device_run": getattr(wl, "e2e_outputs_equal", None),
                 "host": topo,
                 "pipeline": "H2D, kernels and D2H on three streams (each copy direction fanned out over 4 "
                             "side streams in 32 MiB pieces), two device buffer sets"},
