@@ -234,7 +234,8 @@ fp8q_status_t mxfp8_quantize_swizzled_group(const mxfp8_tensor_t* tensors, int c
  * mxfp8_dequantize_swizzled: w = RNE_bf16(decode_e4m3(c) * 2^(e - 127)) for
  *   codes [batch, m, k] and the swizzled E8M0 bytes of mxfp8_quantize_swizzled;
  *   the product is exact, only results below the bf16 range round.
- *   out_bf16: batch*m*k bf16 (out).  Same shape rules as the quantizer.
+ *   out_bf16: batch*m*k bf16 (out).  Same shape rules as the quantizer,
+ *   and batch * ceil(m/128) * ceil(k/128) < 2^32 (FP8Q_ERR_SIZE).
  * mxfp8_unswizzle_scales: the E8M0 bytes in plain row-major order
  *   [batch, m, k/32] (the layout whose trailing k/32 dimension [P3]'s inline
  *   review insists on keeping, even when it is 1).

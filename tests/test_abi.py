@@ -147,6 +147,16 @@ def test_other_entry_points_validation(L):
     assert L.fp8q_dequant_reduce_unfused(c, s, 2, 1024, 0, A + 4 * MB, A + 4 * MB, None, None) == ERR_ALIAS
 
 
+def test_mxfp8_dequantize_tile_count_limit(L):
+    # 2^32 + 5 one-row matrices of k = 32: n stays below the element limit,
+    # but the tile count does not fit the kernel's 32-bit tile index
+    G = 1 << 42                   # address spacing: the scale buffer alone is 2 TiB
+    batch = (1 << 32) + 5
+    assert L.mxfp8_dequantize_swizzled(A, A + G, batch, 1, 32, A + 2 * G, None) == ERR_SIZE
+    assert L.mxfp8_dequantize_swizzled(A, A + G, 4, 1, 48, A + 2 * G, None) == ERR_K
+    assert L.mxfp8_dequantize_swizzled(A, A + G, 0, 1, 32, A + 2 * G, None) == OK
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     import weight_transfer_gb300 as w

@@ -9,8 +9,9 @@
 //   mxfp8_dequantize_swizzled  w = RNE_bf16(decode_e4m3(c) * 2^(e - 127))
 //   mxfp8_unswizzle_scales     swizzled E8M0 bytes -> row-major [batch, m, k/32]
 //   fp8q_count_mismatches      number of differing bytes of two buffers
-// None of them is on the sender's hot path; they are grid-stride kernels with
-// 16-byte accesses.
+// None of them is on the sender's hot path.  The dequantize walks whole
+// 128 x 128 tiles, whose scales are one contiguous 512-byte tile; the other
+// two are grid-stride kernels.
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
@@ -22,33 +23,53 @@ __device__ __forceinline__ int64_t swizzle_offset(int64_t bt, int64_t r, int64_t
            ((r % 128) / 32) * 4 + (j % 4);
 }
 
-// One thread per 16 consecutive codes (half of a 32-element block).
+// Dequantize by whole 128 x 128 tiles of the [batch * m, k] code matrix: the
+// tiles of the swizzled scale layout, so tile t's 512 E8M0 bytes are the
+// contiguous bytes [512 t, 512 t + 512) of the scale buffer.  256 threads
+// per tile: 8 per row, 16 codes each (one 16-byte load, two 16-byte bf16
+// stores), 32 rows per pass, 4 passes.  The tile index is split into
+// (matrix, row tile, column tile) once per tile, in 32-bit arithmetic (the
+// entry point rejects tensors of 2^32 tiles or more).
 __global__ void __launch_bounds__(256)
 mxfp8_dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int64_t m,
-                        int64_t k, size_t units, uint16_t* __restrict__ out) {
+                        int64_t k, uint32_t total_tiles, uint32_t tiles_per_mat, uint32_t col_tiles,
+                        uint16_t* __restrict__ out) {
     dependency_wait();
     allow_dependents();
-    const int64_t kb = k / 32;
-    for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (size_t)gridDim.x * blockDim.x) {
-        const size_t e0 = u * 16;
-        const int64_t row = (int64_t)(e0 / (size_t)k);        // row of the [batch * m, k] view
-        const int64_t col = (int64_t)(e0 - (size_t)row * (size_t)k);
-        const int64_t bt = row / m, r = row - bt * m;
-        const uint32_t e8 = scales[swizzle_offset(bt, r, col / 32, m, kb)];
-        // 2^(e8 - 127): a normal binary32 for e8 >= 1, the subnormal 2^-127 for e8 == 0
-        const float factor = __uint_as_float(e8 ? (e8 << 23) : 0x00400000u);
-        const uint4 c = ld_stream(codes + e0);
-        float d[16];
-        decode_fp8x4<kE4M3>(c.x, d);
-        decode_fp8x4<kE4M3>(c.y, d + 4);
-        decode_fp8x4<kE4M3>(c.z, d + 8);
-        decode_fp8x4<kE4M3>(c.w, d + 12);
-        uint32_t h[8];
+    const unsigned tid = threadIdx.x;
+    const unsigned chunk = tid & 7u;               // 16-code chunk inside the tile row
+    const unsigned rsub = tid >> 3;                // row inside a 32-row pass
+    const unsigned j = chunk >> 1;                 // scale column inside the tile (32 codes)
+    for (uint32_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        const uint32_t bt = t / tiles_per_mat;
+        const uint32_t rem = t - bt * tiles_per_mat;
+        const uint32_t rt = rem / col_tiles;
+        const uint32_t ct = rem - rt * col_tiles;
+        const int64_t col = (int64_t)ct * 128 + chunk * 16;
+        if (col >= k) continue;                    // k % 32 == 0: a chunk is wholly in or out
+        const uint8_t* stile = scales + (size_t)t * 512;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)     // the products are exact; only the bf16 rounding rounds
-            h[i] = pack_bf16x2(__fmul_rn(d[2 * i], factor), __fmul_rn(d[2 * i + 1], factor));
-        st_stream(out + e0, make_uint4(h[0], h[1], h[2], h[3]));
-        st_stream(out + e0 + 8, make_uint4(h[4], h[5], h[6], h[7]));
+        for (int p = 0; p < 4; ++p) {
+            const unsigned r = p * 32 + rsub;      // row inside the tile
+            const int64_t row = (int64_t)rt * 128 + r;
+            if (row >= m) break;                   // later passes are further down
+            const size_t e0 = (size_t)((int64_t)bt * m + row) * (size_t)k + (size_t)col;
+            const uint32_t e8 = __ldg(stile + (r & 31u) * 16 + (r >> 5) * 4 + j);
+            // 2^(e8 - 127): a normal binary32 for e8 >= 1, the subnormal 2^-127 for e8 == 0
+            const float factor = __uint_as_float(e8 ? (e8 << 23) : 0x00400000u);
+            const uint4 c = ld_stream(codes + e0);
+            float d[16];
+            decode_fp8x4<kE4M3>(c.x, d);
+            decode_fp8x4<kE4M3>(c.y, d + 4);
+            decode_fp8x4<kE4M3>(c.z, d + 8);
+            decode_fp8x4<kE4M3>(c.w, d + 12);
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)     // the products are exact; only the bf16 rounding rounds
+                h[i] = pack_bf16x2(__fmul_rn(d[2 * i], factor), __fmul_rn(d[2 * i + 1], factor));
+            st_stream(out + e0, make_uint4(h[0], h[1], h[2], h[3]));
+            st_stream(out + e0 + 8, make_uint4(h[4], h[5], h[6], h[7]));
+        }
     }
 }
 
@@ -108,14 +129,16 @@ extern "C" fp8q_status_t mxfp8_dequantize_swizzled(const uint8_t* codes, const u
     if (!aligned16(codes) || !aligned16(scales_swizzled) || !aligned16(out_bf16)) return FP8Q_ERR_ALIGN;
     const size_t sb = mxfp8_swizzled_scale_bytes(batch, m, k);
     if (overlaps(out_bf16, 2 * n, codes, n) || overlaps(out_bf16, 2 * n, scales_swizzled, sb)) return FP8Q_ERR_ALIAS;
+    const int64_t row_tiles = (m + 127) / 128, col_tiles = (k / MXFP8_BLOCK + 3) / 4;
+    const uint64_t tiles = (uint64_t)batch * (uint64_t)row_tiles * (uint64_t)col_tiles;
+    if (tiles > 0xFFFFFFFFull) return FP8Q_ERR_SIZE;       // the kernel indexes tiles in 32 bits
     static KernelCache kc;
     int resident = 0;
     const fp8q_status_t pst = prepare_kernel(kc, mxfp8_dequantize_kernel, 256, 0, 0, &resident);
     if (pst != FP8Q_OK) return pst;
-    const size_t units = n / 16;
-    return launch(mxfp8_dequantize_kernel, grid_for((units + 255) / 256, resident), 256, 0,
-                  reinterpret_cast<cudaStream_t>(stream), codes, scales_swizzled, m, k, units,
-                  static_cast<uint16_t*>(out_bf16));
+    return launch(mxfp8_dequantize_kernel, grid_for((size_t)tiles, resident), 256, 0,
+                  reinterpret_cast<cudaStream_t>(stream), codes, scales_swizzled, m, k, (uint32_t)tiles,
+                  (uint32_t)(row_tiles * col_tiles), (uint32_t)col_tiles, static_cast<uint16_t*>(out_bf16));
 }
 
 extern "C" fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, int64_t batch, int64_t m, int64_t k,
