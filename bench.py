@@ -873,6 +873,23 @@ def extra_rows(wl, torch, peak):
         "bf16_ring_bytes_per_rank": 2 * (P - 1) * m * 2,
         "wire_saving_vs_bf16": round(1 - wire[0] / (2 * (P - 1) * m * 2), 6)}
     del res, ws
+    # the same collective at 256 MiB of bf16 per rank (device-drawn partials,
+    # N(0, 1e-4^2)): per-rank chunks of 16.8M elements instead of 1.6M
+    nl_ = 8 * (1 << 24)
+    g = torch.Generator(device=dev)
+    g.manual_seed(300)
+    big = [torch.randn(nl_, device=dev, generator=g).mul_(1e-4).to(torch.bfloat16) for _ in range(P)]
+    bres = [torch.empty(nl_, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    bws = torch.empty(int(w.lib().fp8q_ring_allreduce_workspace_bytes(P, nl_)), dtype=torch.uint8, device=dev)
+    ms = timed(torch, st, lambda: w.fp8q_ring_allreduce_sim(big, "e4m3", results=bres, workspace=bws, stream=st),
+               flush)
+    ml = nl_ // P
+    kb2 = P * bytes_quantize(ml) + (P - 1) * P * bytes_hop(ml, False) + P * (nl_ + 4 * nscales(nl_) + 2 * nl_)
+    out["ring_allreduce_sim_256MiB_per_rank"] = {
+        "ranks": P, "elements": nl_, "ms": round(ms, 4), "kernel_bytes": kb2,
+        "GB/s": round(kb2 / (ms * 1e-3) / 1e9, 1), "frac_of_peak": round(kb2 / (ms * 1e-3) / 1e9 / peak, 4)}
+    out["ring_allreduce_sim"]["frac_of_peak"] = round(out["ring_allreduce_sim"]["GB/s"] / peak, 4)
+    del big, bres, bws
     name, b, mm, kk = wl.tensors[0]
     c, sc, sb = ds.mx[0]
     outw = torch.empty((b, mm, kk), dtype=torch.bfloat16, device=dev)
