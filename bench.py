@@ -899,6 +899,32 @@ def extra_rows(wl, torch, peak):
                                "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
                                "frac_of_peak": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
     del outw
+    # NEXT-4: the layer's MXFP8 weights packed with their scales into transfer
+    # buffers of at most 256 MiB (each weight and its scale in one buffer), all
+    # buffers filled by one gather launch, then scattered back by one launch
+    pairs = [(c.numel(), sb_) for c, _, sb_ in ds.mx]
+    slots, sizes = w.fp8q_pack_plan(pairs, 256 << 20)
+    bufs = [torch.empty(sz, dtype=torch.uint8, device=dev) for sz in sizes]
+    outs_c = [torch.empty_like(c) for c, _, _ in ds.mx]
+    outs_s = [torch.empty(sb_, dtype=torch.uint8, device=dev) for _, _, sb_ in ds.mx]
+    gather, scatter = [], []
+    for (bt, co, so), (c, sc_, sb_), oc, os_ in zip(slots, ds.mx, outs_c, outs_s):
+        cv = c.view(-1)
+        gather += [(cv, bufs[bt][co:co + cv.numel()]), (sc_[:sb_], bufs[bt][so:so + sb_])]
+        scatter += [(bufs[bt][co:co + cv.numel()], oc.view(-1)), (bufs[bt][so:so + sb_], os_)]
+    moved = sum(a + b for a, b in pairs)
+    ms_g = timed(torch, st, lambda: w.fp8q_copy_segments(gather, stream=st), flush)
+    ms_s = timed(torch, st, lambda: w.fp8q_copy_segments(scatter, stream=st), flush)
+    torch.cuda.synchronize()
+    same = all(torch.equal(oc, c) for oc, (c, _, _) in zip(outs_c, ds.mx)) and \
+        all(torch.equal(os_, sc_[:sb_]) for os_, (_, sc_, sb_) in zip(outs_s, ds.mx))
+    out["pack_layer"] = {"weights": len(pairs), "buffers": len(sizes), "cap_bytes": 256 << 20, "bytes": moved,
+                         "gather_us": round(1e3 * ms_g, 2), "scatter_us": round(1e3 * ms_s, 2),
+                         "GB/s": round(2 * moved / (ms_g * 1e-3) / 1e9, 1),
+                         "frac_of_peak": round(2 * moved / (ms_g * 1e-3) / 1e9 / peak, 4),
+                         "round_trip_equal": same,
+                         "bytes_counted": "read + written by the gather launch"}
+    del bufs, outs_c, outs_s, gather, scatter
     codes = torch.empty(P * n, dtype=torch.uint8, device=dev)
     sa = torch.empty(4, dtype=torch.float32, device=dev)
     x = ds.bucket.reshape(-1)
