@@ -1023,6 +1023,42 @@ def vec3p5b_row(wl, torch, peak, reps=3):
             "inputs": "device Philox normal, seeds 100 + shard, with the vector's outliers and zero blocks"}
 
 
+def graph_step(wl, torch, reps=50):
+    """The step captured once into a CUDA graph (its own buffer set, on its
+    own stream) and replayed: median step time over `reps` replays, with
+    L2 flushed before each, and whether the replay's results equal a
+    stream-launched step on the same inputs."""
+    dev = wl.dev
+    flush = L2Flush(torch, dev)
+    s = torch.cuda.Stream(dev)
+    ds = DeviceSet(wl, s)
+    wl.h2d(ds, s)
+    with torch.cuda.stream(s):
+        ds.run()                                   # first-call setup outside the capture
+    torch.cuda.synchronize(dev)
+    ref = [o.clone() for o in ds.outputs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ds.run()
+    main = torch.cuda.current_stream(dev)
+    times = []
+    for i in range(reps + 3):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        g.replay()
+        b.record(main)
+        torch.cuda.synchronize(dev)
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    same = all(torch.equal(o.view(-1).view(torch.uint8), r.view(-1).view(torch.uint8)) for o, r in zip(ds.outputs, ref))
+    ms = sorted(times)[len(times) // 2]
+    del g, ds, ref
+    torch.cuda.empty_cache()
+    return {"ms_median": round(ms, 4), "GB/s": round(wl.step_bytes / (ms * 1e-3) / 1e9, 1), "replays": reps,
+            "outputs_equal_stream_run": same}
+
+
 def hbm_copy_check(torch, dev, nbytes=2 << 30, reps=5):
     """A device-to-device copy of `nbytes` on this GPU in the same run (read
     plus written bytes over the median time): the box's own copy rate, shown
@@ -1224,6 +1260,7 @@ def main():
 
     peak, peak_kind = measured_peaks()
     copy_check = hbm_copy_check(torch, dev)
+    graph = graph_step(wl, torch)
     extras = extra_rows(wl, torch, peak)
     if not args.no_vec3p5b:
         extras["vec3p5b"] = vec3p5b_row(wl, torch, peak)
@@ -1259,6 +1296,7 @@ def main():
         "kernels_timing": f"separate pass of {nbreak} steps with events around every launch",
         "segments": [dict(g, frac_of_peak=round(g["GB/s"] / peak, 4)) for g in segments],
         "segments_timing": f"separate pass of {nbreak} steps with events only where the kernel changes",
+        "graph_step": graph,
         "launch_overlap": {"step_ms_on": round(ms_local, 4), "step_ms_off": round(ms_no_overlap, 4),
                            "steps_off": nbreak,
                            "what": "programmatic dependent launch of every kernel (on in the timed steps)"},
