@@ -152,7 +152,8 @@ def measured_peaks():
 
 def kernel_source_hash(name):
     src = {"mxfp8_quantize_kernel": "mxfp8.cu", "quantize_blockwise_kernel": "quantize.cu",
-           "dequant_reduce_kernel": "reduce.cu", "ring_hop_kernel": "ring_hop.cu"}[name]
+           "dequant_reduce_kernel": "reduce.cu", "ring_hop_kernel": "ring_hop.cu",
+           "mxfp8_dequantize_kernel": "mxfp8_receive.cu"}[name]
     h = hashlib.sha256()
     for f in (src, "fp8q_device.cuh"):
         with open(os.path.join(ROOT, "weight_transfer_gb300", "csrc", f), "rb") as fh:
@@ -693,9 +694,20 @@ def run_profile_case(case, launches):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     wl = Workload(dev, 0, torch)
-    kind, first = PROFILE_CASES[case]
     wl.run()                                   # every kernel's inputs exist
     torch.cuda.synchronize()
+    if case == "mxfp8_dequantize":
+        # the receiver side on the step's expert gate batch (outside the step)
+        name, b, mm, kk = wl.tensors[0]
+        c, sc, sb = wl.sets[0].mx[0]
+        out = torch.empty((b, mm, kk), dtype=torch.bfloat16, device=dev)
+        for _ in range(max(1, launches)):
+            wl.w.mxfp8_dequantize_swizzled(c, sc, out=out, stream=wl.stream)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": case, "kernel": "mxfp8_dequantize_kernel", "launches": launches,
+                          "bytes_per_launch": 3 * b * mm * kk + sb}))
+        return
+    kind, first = PROFILE_CASES[case]
     _, nbytes, _, fn, fargs = wl.launches[first]
     assert wl.launches[first][0] == kind
     for _ in range(max(1, launches)):
@@ -1121,7 +1133,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-vec3p5b", action="store_true", help="skip the 3.5e9-element vector row")
-    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES) + ["mxfp8_dequantize"],
                     help="launch one kernel of the step a few times on its bench inputs and exit (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
