@@ -286,11 +286,16 @@ class DeviceSet:
         def add(kind, nbytes, elems, fn, *args):
             launches.append((kind, nbytes, elems, fn, args))
 
+        # FP8Q_INPUTS_READY holds for every launch of the step but the hops:
+        # the bucket and the layer are written only by copies, and each reduce
+        # reads codes that the quantize two launches earlier wrote (a kernel
+        # of the library lets its successor start only after its own wait)
+        ready = ctypes.c_uint(wl.w.FP8Q_INPUTS_READY)
         for f in (0, 1):
             c, sc = self.q[f]
-            add("quantize_blockwise_kernel", bytes_quantize(k * n), k * n, L.fp8q_quantize_blockwise,
+            add("quantize_blockwise_kernel", bytes_quantize(k * n), k * n, L.fp8q_quantize_blockwise_ex,
                 vp(self.bucket.data_ptr()), ctypes.c_size_t(k * n), ctypes.c_int(f), vp(c.data_ptr()),
-                vp(sc.data_ptr()), sp_)
+                vp(sc.data_ptr()), ready, sp_)
         self._keep = []
         for f in (0, 1):
             c, sc = self.q[f]
@@ -298,8 +303,8 @@ class DeviceSet:
             sp = (vp * k)(*[sc[r].data_ptr() for r in range(k)])
             self._keep += [cp, sp]
             ob, of = self.red[f]
-            add("dequant_reduce_kernel", bytes_reduce(n, k), n, L.fp8q_dequant_reduce, cp, sp, ctypes.c_int(k),
-                ctypes.c_size_t(n), ctypes.c_int(f), vp(ob.data_ptr()), vp(of.data_ptr()), sp_)
+            add("dequant_reduce_kernel", bytes_reduce(n, k), n, L.fp8q_dequant_reduce_ex, cp, sp, ctypes.c_int(k),
+                ctypes.c_size_t(n), ctypes.c_int(f), vp(ob.data_ptr()), vp(of.data_ptr()), ready, sp_)
         # hop 0 = e4m3 quantize of rank 0's shard; hop h adds shard h, which
         # only the step's input copy writes, so each hop may start reading it
         # while the previous hop drains
@@ -321,8 +326,8 @@ class DeviceSet:
             self._group[i] = wl.w.mxfp8_tensor_t(x.data_ptr(), b, m, kk, c.data_ptr(), sc.data_ptr())
             mx_bytes += bytes_mxfp8(b, m, kk, sb)
             mx_elems += b * m * kk
-        add("mxfp8_quantize_kernel", mx_bytes, mx_elems, L.mxfp8_quantize_swizzled_group, self._group,
-            ctypes.c_int(len(wl.tensors)), sp_)
+        add("mxfp8_quantize_kernel", mx_bytes, mx_elems, L.mxfp8_quantize_swizzled_group_ex, self._group,
+            ctypes.c_int(len(wl.tensors)), ready, sp_)
         self.launches = launches
 
     def segments(self):

@@ -81,6 +81,22 @@ typedef enum {
 fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, fp8q_format_t fmt,
                                       uint8_t* codes, float* scales, fp8q_stream_t stream);
 
+/* Flag of the *_ex entry points (quantize, dequant-reduce, MXFP8 group):
+ * the caller guarantees that no kernel that can still be running when this
+ * call's kernel starts writes any of the call's inputs.  Every kernel of
+ * this library lets its successor start only after its own grid-dependency
+ * wait, so in a chain of these calls an input written two or more launches
+ * back qualifies.  With programmatic dependent launch on (see
+ * fp8q_set_launch_overlap) the kernel then starts copying its first tiles'
+ * inputs while the previous kernel on the stream is finishing; every write
+ * still waits for it.  Results are unchanged.  Unknown flag bits give
+ * FP8Q_ERR_FLAGS. */
+#define FP8Q_INPUTS_READY 1u
+
+/* fp8q_quantize_blockwise with flags (FP8Q_INPUTS_READY). */
+fp8q_status_t fp8q_quantize_blockwise_ex(const void* x_bf16, size_t n, fp8q_format_t fmt, uint8_t* codes,
+                                         float* scales, unsigned int flags, fp8q_stream_t stream);
+
 /* ---------------------------------------------------------------- (b) ----
  * Fused k-way dequantize-then-reduce ([P1] "FP8 Transmission Optimization
  * and Bottlenecks": the fused kernel never writes dequantized shards to
@@ -94,6 +110,11 @@ fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, fp8q_format_
 fp8q_status_t fp8q_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k,
                                   size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
                                   fp8q_stream_t stream);
+
+/* fp8q_dequant_reduce with flags (FP8Q_INPUTS_READY, see above). */
+fp8q_status_t fp8q_dequant_reduce_ex(const uint8_t* const* codes, const float* const* scales, int k,
+                                     size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
+                                     unsigned int flags, fp8q_stream_t stream);
 
 /* ---------------------------------------------------------------- (c) ----
  * One hop of a ring reduction carried on the FP8 wire format ([P1] ring-based
@@ -227,6 +248,11 @@ typedef struct {
  * count must be in [1, MXFP8_MAX_GROUP] (FP8Q_ERR_SIZE).  Empty tensors are
  * skipped.  Results are those of one mxfp8_quantize_swizzled per tensor. */
 fp8q_status_t mxfp8_quantize_swizzled_group(const mxfp8_tensor_t* tensors, int count, fp8q_stream_t stream);
+
+/* mxfp8_quantize_swizzled_group with flags (FP8Q_INPUTS_READY: no kernel
+ * still running writes any tensor's w_bf16). */
+fp8q_status_t mxfp8_quantize_swizzled_group_ex(const mxfp8_tensor_t* tensors, int count, unsigned int flags,
+                                               fp8q_stream_t stream);
 
 /* ------------------------------------------------------ MXFP8 receiver ----
  * The receiving side of [P3]'s prequantized transfer.

@@ -147,6 +147,22 @@ def test_other_entry_points_validation(L):
     assert L.fp8q_dequant_reduce_unfused(c, s, 2, 1024, 0, A + 4 * MB, A + 4 * MB, None, None) == ERR_ALIAS
 
 
+def test_inputs_ready_flag_validation(L):
+    import weight_transfer_gb300 as w
+    # unknown flag bits are rejected first; the known flag passes the checks
+    assert L.fp8q_quantize_blockwise_ex(A, 1024, 0, A + MB, A + 2 * MB, 2, None) == ERR_FLAGS
+    assert L.fp8q_quantize_blockwise_ex(A, 0, 0, A + MB, A + 2 * MB, w.FP8Q_INPUTS_READY, None) == OK
+    assert L.fp8q_quantize_blockwise_ex(A, 1024, 9, A + MB, A + 2 * MB, w.FP8Q_INPUTS_READY, None) == ERR_FORMAT
+    c = _ptrs([A, A + MB])
+    s = _ptrs([A + 2 * MB, A + 3 * MB])
+    assert L.fp8q_dequant_reduce_ex(c, s, 2, 1024, 0, A + 4 * MB, None, 4, None) == ERR_FLAGS
+    assert L.fp8q_dequant_reduce_ex(c, s, 2, 0, 0, A + 4 * MB, None, w.FP8Q_INPUTS_READY, None) == OK
+    T = w.mxfp8_tensor_t
+    ok = (T * 1)(T(A, 1, 128, 64, A + MB, A + 2 * MB))
+    assert L.mxfp8_quantize_swizzled_group_ex(ok, 1, 8, None) == ERR_FLAGS
+    assert L.mxfp8_quantize_swizzled_group_ex(ok, 0, w.FP8Q_INPUTS_READY, None) == ERR_SIZE
+
+
 def test_mxfp8_dequantize_tile_count_limit(L):
     # 2^32 + 5 one-row matrices of k = 32: n stays below the element limit,
     # but the tile count does not fit the kernel's 32-bit tile index

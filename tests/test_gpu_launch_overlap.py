@@ -156,3 +156,38 @@ def test_ddp_ring_chain_as_the_bench_launches_it(w, orc):
         assert_same(got[h - 1][0], c, f"hop {h} codes")
         assert_same_f32(got[h - 1][1], s, f"hop {h} scales")
     assert_same(bits16(last), eb, "final bf16")
+
+
+def test_step_with_inputs_ready(w, orc):
+    # the bench step's order with FP8Q_INPUTS_READY wherever it holds: both
+    # quantizes read the bucket (written by copies), each reduce reads codes
+    # written two launches back, the MXFP8 group reads weights written by a
+    # copy; results equal the unflagged run and the oracle
+    k, n = 8, 4096 * 9 + 128 * 3 + 77
+    host = [gen.normal_bf16(n, 1e-3, seed=900 + r, outlier_p=1e-3, outlier_mult=100.0) for r in range(k)]
+    mx_shapes = [(2, 256, 768), (1, 384, 96)]
+    mx_host = [gen.normal_bf16(b * m * kk, 0.02, seed=950 + i).view(b, m, kk) for i, (b, m, kk) in enumerate(mx_shapes)]
+    shards = [h.cuda() for h in host]
+    mx_in = [h.cuda() for h in mx_host]
+    torch.cuda.synchronize()
+    res = {}
+    for flags in (w.FP8Q_INPUTS_READY, 0):
+        q = {f: [w.fp8q_quantize_blockwise_ex(x, f, flags) for x in shards] for f in (0, 1)}
+        red = {f: w.fp8q_dequant_reduce_ex([c for c, _ in q[f]], [s for _, s in q[f]], f, flags) for f in (0, 1)}
+        mc, ms = w.mxfp8_quantize_swizzled_group_ex(mx_in, flags)
+        torch.cuda.synchronize()
+        res[flags] = ([u8(c) for f in (0, 1) for c, _ in q[f]], [bits16(red[f][0]) for f in (0, 1)],
+                      [red[f][1].cpu().numpy() for f in (0, 1)], [u8(c) for c in mc], [u8(s) for s in ms])
+    a, b = res[w.FP8Q_INPUTS_READY], res[0]
+    for x, y in zip(a, b):
+        for i, (p_, q_) in enumerate(zip(x, y)):
+            assert np.array_equal(p_.view(np.uint8), q_.view(np.uint8)), f"flagged run differs ({i})"
+    for f in (0, 1):
+        oq = [orc.quantize_blockwise(bits16(h), f) for h in host]
+        eb, ef = orc.dequant_reduce([c for c, _ in oq], [s for _, s in oq], f)
+        assert_same(a[1][f], eb, f"reduce bf16 fmt {f}")
+        assert_same_f32(a[2][f], ef, f"reduce fp32 fmt {f}")
+    for i, (bb, m, kk) in enumerate(mx_shapes):
+        ec, es = orc.mxfp8_quantize_swizzled(bits16(mx_host[i]).ravel(), bb, m, kk)
+        assert_same(a[3][i].ravel(), ec, f"mxfp8 codes {i}")
+        assert_same(a[4][i][:es.size], es, f"mxfp8 scales {i}")

@@ -55,6 +55,7 @@ class fp8q_hop_t(ctypes.Structure):
 
 FP8Q_MAX_HOP_GROUP = 16
 FP8Q_HOP_LOCAL_READY = 1
+FP8Q_INPUTS_READY = 1
 
 
 class mxfp8_tensor_t(ctypes.Structure):
@@ -97,6 +98,10 @@ _SIGNATURES = {
     "fp8q_copy_segments": ([ctypes.POINTER(fp8q_copy_t), _int, _vp], _int),
     "fp8q_ring_hop_group": ([ctypes.POINTER(fp8q_hop_t), _int, _int, _vp], _int),
     "fp8q_ring_hop_group_ex": ([ctypes.POINTER(fp8q_hop_t), _int, _int, ctypes.c_uint, _vp], _int),
+    "fp8q_quantize_blockwise_ex": ([_vp, _sz, _int, _vp, _vp, ctypes.c_uint, _vp], _int),
+    "fp8q_dequant_reduce_ex": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, ctypes.c_uint,
+                                _vp], _int),
+    "mxfp8_quantize_swizzled_group_ex": ([ctypes.POINTER(mxfp8_tensor_t), _int, ctypes.c_uint, _vp], _int),
     "fp8q_ring_allreduce_workspace_bytes": ([_int, _sz], _sz),
     "fp8q_ring_allreduce_sim": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _sz,
                                  ctypes.POINTER(ctypes.c_uint64), _vp], _int),
@@ -193,17 +198,25 @@ def mxfp8_swizzled_scale_bytes(batch: int, m: int, k: int) -> int:
 
 
 def fp8q_quantize_blockwise(x: torch.Tensor, fmt="e4m3", codes: Optional[torch.Tensor] = None,
-                            scales: Optional[torch.Tensor] = None, stream=None):
+                            scales: Optional[torch.Tensor] = None, stream=None, flags: int = 0):
     """bf16 x -> (codes uint8 [n], scales float32 [ceil(n/128)])."""
     n = x.numel()
     if codes is None:
         codes = torch.empty(n, dtype=torch.uint8, device=x.device)
     if scales is None:
         scales = torch.empty(max(fp8q_num_scales(n), 1), dtype=torch.float32, device=x.device)
-    st = lib().fp8q_quantize_blockwise(_dev(x, "x", torch.bfloat16), n, _fmt(fmt), _dev(codes, "codes", torch.uint8, n),
-                                       _dev(scales, "scales", torch.float32, fp8q_num_scales(n)), _stream(stream))
-    _check("fp8q_quantize_blockwise", st)
+    st = lib().fp8q_quantize_blockwise_ex(_dev(x, "x", torch.bfloat16), n, _fmt(fmt),
+                                          _dev(codes, "codes", torch.uint8, n),
+                                          _dev(scales, "scales", torch.float32, fp8q_num_scales(n)), flags,
+                                          _stream(stream))
+    _check("fp8q_quantize_blockwise_ex" if flags else "fp8q_quantize_blockwise", st)
     return codes, scales
+
+
+def fp8q_quantize_blockwise_ex(x: torch.Tensor, fmt="e4m3", flags: int = 0, codes: Optional[torch.Tensor] = None,
+                               scales: Optional[torch.Tensor] = None, stream=None):
+    """fp8q_quantize_blockwise with flags (FP8Q_INPUTS_READY)."""
+    return fp8q_quantize_blockwise(x, fmt, codes=codes, scales=scales, stream=stream, flags=flags)
 
 
 def _ptr_array(ts: Sequence[torch.Tensor], what: str, dtype, numel: int):
@@ -215,7 +228,8 @@ def _ptr_array(ts: Sequence[torch.Tensor], what: str, dtype, numel: int):
 
 def fp8q_dequant_reduce(codes: Sequence[torch.Tensor], scales: Sequence[torch.Tensor], fmt="e4m3",
                         out_bf16: Optional[torch.Tensor] = None, out_fp32: Optional[torch.Tensor] = None,
-                        want_bf16: bool = True, want_fp32: bool = True, n: Optional[int] = None, stream=None):
+                        want_bf16: bool = True, want_fp32: bool = True, n: Optional[int] = None, stream=None,
+                        flags: int = 0):
     """Sum of k FP8 shards in rank order -> (bf16 [n] or None, fp32 [n] or None)."""
     k = len(codes)
     if k != len(scales):
@@ -229,10 +243,16 @@ def fp8q_dequant_reduce(codes: Sequence[torch.Tensor], scales: Sequence[torch.Te
         out_fp32 = torch.empty(n, dtype=torch.float32, device=dev)
     cp = _ptr_array(codes, "codes", torch.uint8, n)
     sp = _ptr_array(scales, "scales", torch.float32, fp8q_num_scales(n))
-    st = lib().fp8q_dequant_reduce(cp, sp, k, n, _fmt(fmt), _dev(out_bf16, "out_bf16", torch.bfloat16, n),
-                                   _dev(out_fp32, "out_fp32", torch.float32, n), _stream(stream))
-    _check("fp8q_dequant_reduce", st)
+    st = lib().fp8q_dequant_reduce_ex(cp, sp, k, n, _fmt(fmt), _dev(out_bf16, "out_bf16", torch.bfloat16, n),
+                                      _dev(out_fp32, "out_fp32", torch.float32, n), flags, _stream(stream))
+    _check("fp8q_dequant_reduce_ex" if flags else "fp8q_dequant_reduce", st)
     return out_bf16, out_fp32
+
+
+def fp8q_dequant_reduce_ex(codes: Sequence[torch.Tensor], scales: Sequence[torch.Tensor], fmt="e4m3", flags: int = 0,
+                           **kw):
+    """fp8q_dequant_reduce with flags (FP8Q_INPUTS_READY); keyword arguments as fp8q_dequant_reduce."""
+    return fp8q_dequant_reduce(codes, scales, fmt, flags=flags, **kw)
 
 
 def fp8q_ring_hop(in_codes: torch.Tensor, in_scales: torch.Tensor, local: torch.Tensor, fmt="e4m3",
@@ -343,7 +363,7 @@ def fp8q_ring_allreduce_sim(partials: Sequence[torch.Tensor], fmt="e4m3", result
 
 
 def mxfp8_quantize_swizzled_group(weights: Sequence[torch.Tensor], codes: Optional[Sequence[torch.Tensor]] = None,
-                                  scales: Optional[Sequence[torch.Tensor]] = None, stream=None):
+                                  scales: Optional[Sequence[torch.Tensor]] = None, stream=None, flags: int = 0):
     """Several bf16 weights ([m, k] or [batch, m, k]) in one launch ->
     (list of codes, list of swizzled scale buffers), as one
     mxfp8_quantize_swizzled per weight would give."""
@@ -367,9 +387,15 @@ def mxfp8_quantize_swizzled_group(weights: Sequence[torch.Tensor], codes: Option
                                 _dev(sc, f"scales[{i}]", torch.uint8, sb))
         outc.append(c)
         outs.append(sc[:sb])
-    st = lib().mxfp8_quantize_swizzled_group(arr, n, _stream(stream))
-    _check("mxfp8_quantize_swizzled_group", st)
+    st = lib().mxfp8_quantize_swizzled_group_ex(arr, n, flags, _stream(stream))
+    _check("mxfp8_quantize_swizzled_group_ex" if flags else "mxfp8_quantize_swizzled_group", st)
     return outc, outs
+
+
+def mxfp8_quantize_swizzled_group_ex(weights: Sequence[torch.Tensor], flags: int = 0, **kw):
+    """mxfp8_quantize_swizzled_group with flags (FP8Q_INPUTS_READY); keyword
+    arguments as mxfp8_quantize_swizzled_group."""
+    return mxfp8_quantize_swizzled_group(weights, flags=flags, **kw)
 
 
 def _mx_shape(codes: torch.Tensor):

@@ -58,6 +58,7 @@ struct MxGroup {
     uint8_t* codes[kMxMaxGroup];
     uint8_t* scales[kMxMaxGroup];
     int count;
+    int inputs_ready;                       // the weights may be read before the predecessor grid ends
 };
 
 // Which tensor of the group global tile t belongs to (CTA-uniform).
@@ -84,9 +85,6 @@ mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
         for (int s = 0; s < kMxStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
-    dependency_wait();
-    allow_dependents();
-    __syncthreads();
     auto issue = [&](int64_t t, int s) {          // thread 0 only
         const int gi = group_of(g, t);
         const int64_t local = t - g.tile_start[gi];
@@ -98,11 +96,19 @@ mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
         tma_2d_g2s(smem + (size_t)s * kMxStageBytes, &g.tmap[gi], (int)(ct * 128), (int)(bt * g.m[gi] + rt * 128),
                    &full[s]);
     };
-    if (tid == 0)
+    auto prologue = [&]() {                       // thread 0 only: the first tiles
         for (int s = 0; s < kMxStages; ++s) {
             const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
             if (t < total_tiles) issue(t, s);
         }
+    };
+    // with inputs_ready the caller guarantees that no kernel still running
+    // writes the weights: the first tiles are requested before the wait
+    if (tid == 0 && g.inputs_ready) prologue();
+    dependency_wait();
+    allow_dependents();
+    __syncthreads();
+    if (tid == 0 && !g.inputs_ready) prologue();
 
     int it = 0;
     bool failed = false;
@@ -227,7 +233,8 @@ static void tensor_ranges(const mxfp8_tensor_t& t, const void* p[3], size_t sz[3
     sz[2] = mxfp8_swizzled_scale_bytes(t.batch, t.m, t.k);
 }
 
-static fp8q_status_t launch_group(const mxfp8_tensor_t* tensors, int count, cudaStream_t stream) {
+static fp8q_status_t launch_group(const mxfp8_tensor_t* tensors, int count, cudaStream_t stream, unsigned flags = 0) {
+    if (flags & ~FP8Q_INPUTS_READY) return FP8Q_ERR_FLAGS;
     if (!tensors) return FP8Q_ERR_NULL;
     if (count < 1 || count > kMxMaxGroup) return FP8Q_ERR_SIZE;
     int64_t tiles[kMxMaxGroup];
@@ -286,6 +293,7 @@ static fp8q_status_t launch_group(const mxfp8_tensor_t* tensors, int count, cuda
     if (used == 0) return FP8Q_OK;
     g.tile_start[used] = start;
     g.count = used;
+    g.inputs_ready = (flags & FP8Q_INPUTS_READY) ? 1 : 0;
     static KernelCache kc;
     int resident = 0;
     const fp8q_status_t st = prepare_kernel(kc, mxfp8_quantize_kernel, kMxThreads, kMxSmem, kMxSmem, &resident);
@@ -305,4 +313,9 @@ extern "C" fp8q_status_t mxfp8_quantize_swizzled(const void* w_bf16, int64_t bat
 extern "C" fp8q_status_t mxfp8_quantize_swizzled_group(const mxfp8_tensor_t* tensors, int count,
                                                        fp8q_stream_t stream) {
     return launch_group(tensors, count, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8q_status_t mxfp8_quantize_swizzled_group_ex(const mxfp8_tensor_t* tensors, int count,
+                                                          unsigned int flags, fp8q_stream_t stream) {
+    return launch_group(tensors, count, reinterpret_cast<cudaStream_t>(stream), flags);
 }

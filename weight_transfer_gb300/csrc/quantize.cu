@@ -56,7 +56,7 @@ __device__ __forceinline__ void quantize_block16(const uint4& va, const uint4& v
 template <int FMT>
 __global__ void __launch_bounds__(kQuantThreads)
 quantize_blockwise_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __restrict__ codes,
-                          float* __restrict__ scales) {
+                          float* __restrict__ scales, int inputs_ready) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuantStages * kQuantStageBytes);
     const size_t nb = (n + 127) >> 7;
@@ -70,18 +70,23 @@ quantize_blockwise_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __r
         for (int s = 0; s < kQuantStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
-    dependency_wait();
-    allow_dependents();
-    __syncthreads();
     auto issue = [&](size_t t, int s) {           // thread 0 only
         mbar_arrive_expect_tx(&full[s], kQuantStageBytes);
         bulk_g2s(smem + (size_t)s * kQuantStageBytes, x + t * kQuantTile, kQuantStageBytes, &full[s]);
     };
-    if (tid == 0)
+    auto prologue = [&]() {                       // thread 0 only: the first tiles
         for (int s = 0; s < kQuantStages; ++s) {
             const size_t t = blockIdx.x + (size_t)s * gridDim.x;
             if (t < nstaged) issue(t, s);
         }
+    };
+    // with inputs_ready the caller guarantees that no kernel still running
+    // writes x: the first tiles are requested before the grid-dependency wait
+    if (tid == 0 && inputs_ready) prologue();
+    dependency_wait();
+    allow_dependents();
+    __syncthreads();
+    if (tid == 0 && !inputs_ready) prologue();
 
     int it = 0;
     bool failed = false;
@@ -160,7 +165,7 @@ encode_f32_kernel(const float* __restrict__ x, size_t n, uint8_t* __restrict__ c
 
 template <int FMT>
 static fp8q_status_t launch_quantize(const uint16_t* x, size_t n, uint8_t* codes, float* scales,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, int inputs_ready) {
     static KernelCache kc;
     int resident = 0;
     const fp8q_status_t st = prepare_kernel(kc, quantize_blockwise_kernel<FMT>, kQuantThreads, kQuantSmem,
@@ -168,7 +173,8 @@ static fp8q_status_t launch_quantize(const uint16_t* x, size_t n, uint8_t* codes
     if (st != FP8Q_OK) return st;
     const size_t tiles = (n + kQuantTile - 1) / kQuantTile;
     const unsigned grid = grid_for(tiles, resident);
-    return launch(quantize_blockwise_kernel<FMT>, grid, kQuantThreads, kQuantSmem, stream, x, n, codes, scales);
+    return launch(quantize_blockwise_kernel<FMT>, grid, kQuantThreads, kQuantSmem, stream, x, n, codes, scales,
+                  inputs_ready);
 }
 
 template <int FMT>
@@ -190,8 +196,9 @@ unsigned unit_errors_quantize(bool clear) { return read_unit_errors(clear); }
 
 using namespace fp8q;
 
-extern "C" fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, fp8q_format_t fmt,
-                                                 uint8_t* codes, float* scales, fp8q_stream_t stream) {
+static fp8q_status_t quantize_entry(const void* x_bf16, size_t n, fp8q_format_t fmt, uint8_t* codes, float* scales,
+                                    unsigned flags, fp8q_stream_t stream) {
+    if (flags & ~FP8Q_INPUTS_READY) return FP8Q_ERR_FLAGS;
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
     if (n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
     if (n == 0) return FP8Q_OK;
@@ -203,8 +210,20 @@ extern "C" fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, f
         return FP8Q_ERR_ALIAS;
     const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return fmt == FP8Q_E4M3 ? launch_quantize<kE4M3>(x, n, codes, scales, s)
-                            : launch_quantize<kE5M2>(x, n, codes, scales, s);
+    const int ready = (flags & FP8Q_INPUTS_READY) ? 1 : 0;
+    return fmt == FP8Q_E4M3 ? launch_quantize<kE4M3>(x, n, codes, scales, s, ready)
+                            : launch_quantize<kE5M2>(x, n, codes, scales, s, ready);
+}
+
+extern "C" fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, fp8q_format_t fmt,
+                                                 uint8_t* codes, float* scales, fp8q_stream_t stream) {
+    return quantize_entry(x_bf16, n, fmt, codes, scales, 0, stream);
+}
+
+extern "C" fp8q_status_t fp8q_quantize_blockwise_ex(const void* x_bf16, size_t n, fp8q_format_t fmt,
+                                                    uint8_t* codes, float* scales, unsigned int flags,
+                                                    fp8q_stream_t stream) {
+    return quantize_entry(x_bf16, n, fmt, codes, scales, flags, stream);
 }
 
 extern "C" fp8q_status_t fp8q_encode_f32(const float* x, size_t n, fp8q_format_t fmt, uint8_t* codes,

@@ -83,7 +83,8 @@ __device__ __forceinline__ void store16(const float (&acc)[16], size_t e0, size_
 // of the unrolled iterations are switched off).
 template <int FMT, bool OUT_BF16, bool OUT_F32, bool SUM, int KMAX>
 __global__ void __launch_bounds__(kRedThreads)
-dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32) {
+dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_bf16, float* __restrict__ out_f32,
+                      int inputs_ready) {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t stage_bytes = red_stage_bytes(k);
     const uint32_t codes_bytes = (uint32_t)k * kRedTile;
@@ -96,10 +97,6 @@ dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_
         for (int s = 0; s < kRedStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
-    dependency_wait();
-    allow_dependents();
-    __syncthreads();
-
     auto issue = [&](size_t t, int s) {           // thread 0 only
         uint8_t* st = smem + (size_t)s * stage_bytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
@@ -109,11 +106,19 @@ dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_
                      4 * kRedTile / 128, &full[s]);
         }
     };
-    if (tid == 0)
+    auto prologue = [&]() {                       // thread 0 only: the first tiles
         for (int s = 0; s < kRedStages; ++s) {
             const size_t t = blockIdx.x + (size_t)s * gridDim.x;
             if (t < nstaged) issue(t, s);
         }
+    };
+    // with inputs_ready the caller guarantees that no kernel still running
+    // writes the shards: the first tiles are requested before the wait
+    if (tid == 0 && inputs_ready) prologue();
+    dependency_wait();
+    allow_dependents();
+    __syncthreads();
+    if (tid == 0 && !inputs_ready) prologue();
 
     int it = 0;
     bool failed = false;
@@ -233,7 +238,8 @@ sum_f32_kernel(const float* __restrict__ ws, int k, size_t n, size_t slot, uint1
 }
 
 template <int FMT, bool B, bool F, bool SUM, int KMAX>
-static fp8q_status_t launch_reduce_k(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
+static fp8q_status_t launch_reduce_k(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s,
+                                     int ready) {
     auto kernel = dequant_reduce_kernel<FMT, B, F, SUM, KMAX>;
     // one cache per shard count: the stage size, and so the occupancy, depends on k
     static KernelCache kc[KMAX + 1];
@@ -243,26 +249,28 @@ static fp8q_status_t launch_reduce_k(const ShardPtrs& sh, int k, size_t n, uint1
     if (st != FP8Q_OK) return st;
     const size_t tiles = (n + kRedTile - 1) / kRedTile;
     const unsigned grid = grid_for(tiles, resident);
-    return launch(kernel, grid, kRedThreads, smem, s, sh, k, n, ob, of);
+    return launch(kernel, grid, kRedThreads, smem, s, sh, k, n, ob, of, ready);
 }
 
 template <int FMT, bool B, bool F, bool SUM>
-static fp8q_status_t launch_reduce_t(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
+static fp8q_status_t launch_reduce_t(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s,
+                                     int ready) {
     if constexpr (!SUM) {
-        return launch_reduce_k<FMT, B, F, SUM, 1>(sh, k, n, ob, of, s);
+        return launch_reduce_k<FMT, B, F, SUM, 1>(sh, k, n, ob, of, s, ready);
     } else {
-        if (k <= 2) return launch_reduce_k<FMT, B, F, SUM, 2>(sh, k, n, ob, of, s);
-        if (k <= 4) return launch_reduce_k<FMT, B, F, SUM, 4>(sh, k, n, ob, of, s);
-        if (k <= 8) return launch_reduce_k<FMT, B, F, SUM, 8>(sh, k, n, ob, of, s);
-        return launch_reduce_k<FMT, B, F, SUM, 16>(sh, k, n, ob, of, s);
+        if (k <= 2) return launch_reduce_k<FMT, B, F, SUM, 2>(sh, k, n, ob, of, s, ready);
+        if (k <= 4) return launch_reduce_k<FMT, B, F, SUM, 4>(sh, k, n, ob, of, s, ready);
+        if (k <= 8) return launch_reduce_k<FMT, B, F, SUM, 8>(sh, k, n, ob, of, s, ready);
+        return launch_reduce_k<FMT, B, F, SUM, 16>(sh, k, n, ob, of, s, ready);
     }
 }
 
 template <int FMT, bool SUM>
-static fp8q_status_t launch_reduce(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s) {
-    if (ob && of) return launch_reduce_t<FMT, true, true, SUM>(sh, k, n, ob, of, s);
-    if (ob) return launch_reduce_t<FMT, true, false, SUM>(sh, k, n, ob, of, s);
-    return launch_reduce_t<FMT, false, true, SUM>(sh, k, n, ob, of, s);
+static fp8q_status_t launch_reduce(const ShardPtrs& sh, int k, size_t n, uint16_t* ob, float* of, cudaStream_t s,
+                                   int ready = 0) {
+    if (ob && of) return launch_reduce_t<FMT, true, true, SUM>(sh, k, n, ob, of, s, ready);
+    if (ob) return launch_reduce_t<FMT, true, false, SUM>(sh, k, n, ob, of, s, ready);
+    return launch_reduce_t<FMT, false, true, SUM>(sh, k, n, ob, of, s, ready);
 }
 
 template <bool B, bool F>
@@ -315,16 +323,30 @@ using namespace fp8q;
 
 extern "C" size_t fp8q_unfused_stride(size_t n) { return (n + 3) & ~(size_t)3; }
 
-extern "C" fp8q_status_t fp8q_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k,
-                                             size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
-                                             fp8q_stream_t stream) {
+static fp8q_status_t reduce_entry(const uint8_t* const* codes, const float* const* scales, int k, size_t n,
+                                  fp8q_format_t fmt, void* out_bf16, float* out_fp32, unsigned flags,
+                                  fp8q_stream_t stream) {
+    if (flags & ~FP8Q_INPUTS_READY) return FP8Q_ERR_FLAGS;
     ShardPtrs sh;
     fp8q_status_t st = check_shards(codes, scales, k, n, fmt, out_bf16, out_fp32, &sh);
     if (st != FP8Q_OK || n == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint16_t* ob = static_cast<uint16_t*>(out_bf16);
-    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, true>(sh, k, n, ob, out_fp32, s)
-                            : launch_reduce<kE5M2, true>(sh, k, n, ob, out_fp32, s);
+    const int ready = (flags & FP8Q_INPUTS_READY) ? 1 : 0;
+    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, true>(sh, k, n, ob, out_fp32, s, ready)
+                            : launch_reduce<kE5M2, true>(sh, k, n, ob, out_fp32, s, ready);
+}
+
+extern "C" fp8q_status_t fp8q_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k,
+                                             size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
+                                             fp8q_stream_t stream) {
+    return reduce_entry(codes, scales, k, n, fmt, out_bf16, out_fp32, 0, stream);
+}
+
+extern "C" fp8q_status_t fp8q_dequant_reduce_ex(const uint8_t* const* codes, const float* const* scales, int k,
+                                                size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
+                                                unsigned int flags, fp8q_stream_t stream) {
+    return reduce_entry(codes, scales, k, n, fmt, out_bf16, out_fp32, flags, stream);
 }
 
 extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
