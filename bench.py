@@ -1040,40 +1040,52 @@ def vec3p5b_row(wl, torch, peak, reps=3):
             "inputs": "device Philox normal, seeds 100 + shard, with the vector's outliers and zero blocks"}
 
 
-def graph_step(wl, torch, reps=50):
-    """The step captured once into a CUDA graph (its own buffer set, on its
-    own stream) and replayed: median step time over `reps` replays, with
-    L2 flushed before each, and whether the replay's results equal a
-    stream-launched step on the same inputs."""
+def graph_timed(wl, torch, flush, steps, dom, barrier, clocks):
+    """K replays of the step captured once as a CUDA graph, on its own buffer
+    set and stream, with the dominant kernel bracketed by event nodes
+    captured in the graph (external events).  L2 is flushed before every
+    replay, outside the step events.  Returns (timing dict, None), or
+    (None, reason) where this torch cannot record events inside a graph."""
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None, "torch.cuda.Event has no external (graph-node) events"
     dev = wl.dev
-    flush = L2Flush(torch, dev)
     s = torch.cuda.Stream(dev)
     ds = DeviceSet(wl, s)
     wl.h2d(ds, s)
     with torch.cuda.stream(s):
         ds.run()                                   # first-call setup outside the capture
     torch.cuda.synchronize(dev)
-    ref = [o.clone() for o in ds.outputs]
+    nl = len(ds.launches)
+    dom_ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2 * nl)]
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        ds.run()
+        ds.run(dom_ev, only=dom)
     main = torch.cuda.current_stream(dev)
-    times = []
-    for i in range(reps + 3):
+    dom_idx = [j for j, l in enumerate(ds.launches) if l[0] == dom]
+    step_ms, dom_ms = [], []
+    g.replay()                                     # one untimed replay
+    torch.cuda.synchronize(dev)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
         flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(main)
         g.replay()
         b.record(main)
-        torch.cuda.synchronize(dev)
-        if i >= 3:
-            times.append(a.elapsed_time(b))
-    same = all(torch.equal(o.view(-1).view(torch.uint8), r.view(-1).view(torch.uint8)) for o, r in zip(ds.outputs, ref))
-    ms = sorted(times)[len(times) // 2]
-    del g, ds, ref
+        torch.cuda.synchronize(dev)                # the graph's events are re-recorded by every replay
+        step_ms.append(a.elapsed_time(b))
+        dom_ms += [dom_ev[2 * j].elapsed_time(dom_ev[2 * j + 1]) for j in dom_idx]
+    barrier()
+    t1 = time.perf_counter()
+    same = all(torch.equal(o.contiguous().view(-1).view(torch.uint8), r.contiguous().view(-1).view(torch.uint8))
+               for o, r in zip(ds.outputs, wl.sets[0].outputs))
+    del g, ds
     torch.cuda.empty_cache()
-    return {"ms_median": round(ms, 4), "GB/s": round(wl.step_bytes / (ms * 1e-3) / 1e9, 1), "replays": reps,
-            "outputs_equal_stream_run": same}
+    return {"ms_mean": sum(step_ms) / steps, "ms_median": sorted(step_ms)[steps // 2], "dom_ms": dom_ms,
+            "outputs_equal_stream_run": same, "clocks": clocks.summary(t0, t1)}, None
 
 
 def hbm_copy_check(torch, dev, nbytes=2 << 30, reps=5):
@@ -1242,6 +1254,23 @@ def main():
                 dom_ms += launch_ev[i][2 * j].elapsed_time(launch_ev[i][2 * j + 1])
                 dom_launches += 1
     dom_bytes = per_kind[dom]["bytes"] // per_kind[dom]["launches"]
+    stream_timing = {"ms_per_step": round(ms_local, 4), "GB/s": round(wl.step_bytes / (ms_local * 1e-3) / 1e9, 1),
+                     "dominant_kernel_avg_us": round(1e3 * dom_ms / dom_launches, 2), "clocks": clock_info}
+
+    # ---------------- timed region, graph form: K replays of the step -------
+    graph, graph_why = graph_timed(wl, torch, flush, steps, dom, barrier, clocks)
+    if graph is not None and graph["outputs_equal_stream_run"]:
+        headline = "cuda_graph"
+        ms_local = graph["ms_mean"]
+        dom_ms, dom_launches = sum(graph["dom_ms"]), len(graph["dom_ms"])
+        clock_info = graph["clocks"]
+    else:
+        headline = "stream"
+    graph_timing = ({"unavailable": graph_why} if graph is None else
+                    {"ms_per_step": round(graph["ms_mean"], 4), "ms_median": round(graph["ms_median"], 4),
+                     "GB/s": round(wl.step_bytes / (graph["ms_mean"] * 1e-3) / 1e9, 1),
+                     "dominant_kernel_avg_us": round(1e3 * sum(graph["dom_ms"]) / max(1, len(graph["dom_ms"])), 2),
+                     "outputs_equal_stream_run": graph["outputs_equal_stream_run"], "clocks": graph["clocks"]})
 
     # the same steps with programmatic dependent launch switched off
     wl.w.fp8q_set_launch_overlap(False)
@@ -1277,7 +1306,6 @@ def main():
 
     peak, peak_kind = measured_peaks()
     copy_check = hbm_copy_check(torch, dev)
-    graph = graph_step(wl, torch)
     extras = extra_rows(wl, torch, peak)
     if not args.no_vec3p5b:
         extras["vec3p5b"] = vec3p5b_row(wl, torch, peak)
@@ -1308,13 +1336,16 @@ def main():
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "avg_us": round(1e3 * dom_ms / dom_launches, 2),
                      "copy_check": copy_check,
-                     "timing": "events around each launch of this kernel in the K timed steps"},
+                     "timing": f"events around each launch of this kernel in the K timed steps ({headline} form)"},
         "kernels": kernels,
         "kernels_timing": f"separate pass of {nbreak} steps with events around every launch",
         "segments": [dict(g, frac_of_peak=round(g["GB/s"] / peak, 4)) for g in segments],
         "segments_timing": f"separate pass of {nbreak} steps with events only where the kernel changes",
-        "graph_step": graph,
-        "launch_overlap": {"step_ms_on": round(ms_local, 4), "step_ms_off": round(ms_no_overlap, 4),
+        "timing": {"headline": headline,
+                   "what": "value, ms_per_step and the roofline come from the headline form; both forms run K "
+                           "steps with L2 flushed before each, outside the step events",
+                   "stream": stream_timing, "cuda_graph": graph_timing},
+        "launch_overlap": {"step_ms_on": stream_timing["ms_per_step"], "step_ms_off": round(ms_no_overlap, 4),
                            "steps_off": nbreak,
                            "what": "programmatic dependent launch of every kernel (on in the timed steps)"},
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
