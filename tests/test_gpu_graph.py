@@ -51,13 +51,17 @@ class Step:
             self.mx_in[i].copy_(gen.normal_bf16(b * m * k, 0.02, seed=seed + 50 + i).view(b, m, k))
 
     def launch(self):
+        # the flags where they hold, as the bench's step uses them: the
+        # bucket and the MXFP8 inputs are written by copies only; each reduce
+        # reads codes from quantizes at least two launches back
         w = self.w
+        ready = w.FP8Q_INPUTS_READY
         for f in (0, 1):
             for r in range(K):
-                w.fp8q_quantize_blockwise(self.bucket[r], f, codes=self.q[f][r][0], scales=self.q[f][r][1])
+                w.fp8q_quantize_blockwise_ex(self.bucket[r], f, ready, codes=self.q[f][r][0], scales=self.q[f][r][1])
         for f in (0, 1):
-            w.fp8q_dequant_reduce([c for c, _ in self.q[f]], [s for _, s in self.q[f]], f,
-                                  out_bf16=self.red[f][0], out_fp32=self.red[f][1])
+            w.fp8q_dequant_reduce_ex([c for c, _ in self.q[f]], [s for _, s in self.q[f]], f, ready,
+                                     out_bf16=self.red[f][0], out_fp32=self.red[f][1])
         prev = self.q[0][0]
         for h in range(1, K):
             oc, os_ = self.hops[h - 1]
@@ -65,7 +69,7 @@ class Step:
                   "out_scales": os_, "out_bf16": self.ring_bf16 if h == K - 1 else None}
             w.fp8q_ring_hop_group_ex([hp], 0, w.FP8Q_HOP_LOCAL_READY)
             prev = (oc, os_)
-        w.mxfp8_quantize_swizzled_group(self.mx_in, codes=self.mx_c, scales=self.mx_s)
+        w.mxfp8_quantize_swizzled_group_ex(self.mx_in, ready, codes=self.mx_c, scales=self.mx_s)
         w.fp8q_quantize_tensorwise(self.red[0][0], 0, codes=self.tw_c, scale_amax=self.tw_sa)
 
     def outputs(self):
