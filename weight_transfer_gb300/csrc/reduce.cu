@@ -349,8 +349,10 @@ extern "C" fp8q_status_t fp8q_dequant_reduce_ex(const uint8_t* const* codes, con
     return reduce_entry(codes, scales, k, n, fmt, out_bf16, out_fp32, flags, stream);
 }
 
-extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
-                                         void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
+namespace fp8q {
+fp8q_status_t dequantize_entry(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                               void* out_bf16, float* out_fp32, unsigned flags, fp8q_stream_t stream) {
+    if (flags & ~FP8Q_INPUTS_READY) return FP8Q_ERR_FLAGS;
     ShardPtrs sh;
     const uint8_t* c[1] = {codes};
     const float* sc[1] = {scales};
@@ -358,8 +360,15 @@ extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scal
     if (st != FP8Q_OK || n == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint16_t* ob = static_cast<uint16_t*>(out_bf16);
-    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(sh, 1, n, ob, out_fp32, s)
-                            : launch_reduce<kE5M2, false>(sh, 1, n, ob, out_fp32, s);
+    const int ready = (flags & FP8Q_INPUTS_READY) ? 1 : 0;
+    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(sh, 1, n, ob, out_fp32, s, ready)
+                            : launch_reduce<kE5M2, false>(sh, 1, n, ob, out_fp32, s, ready);
+}
+}  // namespace fp8q
+
+extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                                         void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
+    return dequantize_entry(codes, scales, n, fmt, out_bf16, out_fp32, 0, stream);
 }
 
 extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const float* const* scales,

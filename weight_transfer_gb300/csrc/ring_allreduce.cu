@@ -90,10 +90,13 @@ extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, vo
         return static_cast<const uint16_t*>(base) + (size_t)c * m;
     };
 
-    // reduce-scatter, step 0: every rank quantizes its own chunk
+    // reduce-scatter, step 0: every rank quantizes its own chunk.  From the
+    // second quantize on, the partials' writer (the caller's work) is at
+    // least two launches back, so the inputs may be copied early.
     for (int i = 0; i < ranks; ++i) {
-        const fp8q_status_t st = fp8q_quantize_blockwise(chunk(partials[i], i), m, fmt, msg_codes(0, i),
-                                                         msg_scales(0, i), stream);
+        const fp8q_status_t st = fp8q_quantize_blockwise_ex(chunk(partials[i], i), m, fmt, msg_codes(0, i),
+                                                            msg_scales(0, i), i > 0 ? FP8Q_INPUTS_READY : 0u,
+                                                            stream);
         if (st != FP8Q_OK) return st;
     }
     // steps 1 .. P-1: one hop per rank, all ranks in one launch
@@ -124,8 +127,11 @@ extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, vo
         if (st != FP8Q_OK) return st;
     }
     // all-gather of the reduced codes, then every rank decodes the whole vector
+    // (the last hop group wrote the reduced codes; from the second dequantize
+    // on it is at least two launches back)
     for (int r = 0; r < ranks; ++r) {
-        const fp8q_status_t st = fp8q_dequantize(fin_codes, fin_scales, n, fmt, results[r], nullptr, stream);
+        const fp8q_status_t st = dequantize_entry(fin_codes, fin_scales, n, fmt, results[r], nullptr,
+                                                  r > 0 ? FP8Q_INPUTS_READY : 0u, stream);
         if (st != FP8Q_OK) return st;
     }
     if (wire_bytes) *wire_bytes = 2ull * (uint64_t)(ranks - 1) * (uint64_t)(m + 4 * (m / 128));
