@@ -97,6 +97,26 @@ fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, fp8q_format_
 fp8q_status_t fp8q_quantize_blockwise_ex(const void* x_bf16, size_t n, fp8q_format_t fmt, uint8_t* codes,
                                          float* scales, unsigned int flags, fp8q_stream_t stream);
 
+/* One item of a grouped quantize: the arguments of fp8q_quantize_blockwise. */
+typedef struct {
+    const void* x_bf16;        /* n bf16 (in)                                  */
+    size_t n;
+    uint8_t* codes;            /* n codes (out)                                */
+    float* scales;             /* fp8q_num_scales(n) scales (out)              */
+} fp8q_quant_t;
+
+#define FP8Q_MAX_QUANT_GROUP 16
+
+/* fp8q_quantize_blockwise for up to FP8Q_MAX_QUANT_GROUP independent arrays
+ * in one launch (for instance every rank's chunk of a ring step, or several
+ * gradient buckets).  `items` is a HOST array; every item is checked as by
+ * fp8q_quantize_blockwise, no output may overlap any input or output of the
+ * group (FP8Q_ERR_ALIAS), count must be in [1, FP8Q_MAX_QUANT_GROUP]
+ * (FP8Q_ERR_SIZE), and flags may hold FP8Q_INPUTS_READY.  Empty items are
+ * skipped.  Results are those of one fp8q_quantize_blockwise per item. */
+fp8q_status_t fp8q_quantize_blockwise_group(const fp8q_quant_t* items, int count, fp8q_format_t fmt,
+                                            unsigned int flags, fp8q_stream_t stream);
+
 /* ---------------------------------------------------------------- (b) ----
  * Fused k-way dequantize-then-reduce ([P1] "FP8 Transmission Optimization
  * and Bottlenecks": the fused kernel never writes dequantized shards to

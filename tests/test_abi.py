@@ -163,6 +163,29 @@ def test_inputs_ready_flag_validation(L):
     assert L.mxfp8_quantize_swizzled_group_ex(ok, 0, w.FP8Q_INPUTS_READY, None) == ERR_SIZE
 
 
+def test_quantize_group_validation(L):
+    import weight_transfer_gb300 as w
+    Q = w.fp8q_quant_t
+    g = L.fp8q_quantize_blockwise_group
+    ok = Q(A, 1024, A + MB, A + 2 * MB)
+    arr = (Q * 17)(*([ok] * 17))
+    assert g(arr, 0, 0, 0, None) == ERR_SIZE
+    assert g(arr, 17, 0, 0, None) == ERR_SIZE
+    assert g(arr, 1, 9, 0, None) == ERR_FORMAT
+    assert g(arr, 1, 0, 2, None) == ERR_FLAGS
+    assert g(None, 1, 0, 0, None) == ERR_NULL
+    # item 1 writes its codes over item 0's input
+    alias = (Q * 2)(ok, Q(A + 10 * MB, 1024, A + 512, A + 12 * MB))
+    assert g(alias, 2, 0, 0, None) == ERR_ALIAS
+    # two items writing the same scales
+    same = (Q * 2)(ok, Q(A + 10 * MB, 1024, A + 11 * MB, A + 2 * MB))
+    assert g(same, 2, 0, 0, None) == ERR_ALIAS
+    bad = (Q * 2)(ok, Q(A + 10 * MB + 8, 1024, A + 11 * MB, A + 12 * MB))
+    assert g(bad, 2, 0, 0, None) == ERR_ALIGN
+    empty = (Q * 2)(Q(None, 0, None, None), Q(None, 0, None, None))
+    assert g(empty, 2, 0, w.FP8Q_INPUTS_READY, None) == OK
+
+
 def test_mxfp8_dequantize_tile_count_limit(L):
     # 2^32 + 5 one-row matrices of k = 32: n stays below the element limit,
     # but the tile count does not fit the kernel's 32-bit tile index

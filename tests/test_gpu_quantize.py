@@ -113,3 +113,27 @@ def test_encode_f32_all_2_32_patterns(w, orc, fmt):
         else:
             assert (((g & 0x7C) == 0x7C) & ((g & 3) != 0)).all()
     pool.shutdown()
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("flags", [0, 1])
+def test_quantize_group_mixed_sizes(w, orc, fmt, flags):
+    # items of every shape: a single element, one partial block, whole tiles,
+    # a ragged tile in the middle of the group's tile sequence, an empty item
+    # and large varied inputs; each equals one fp8q_quantize_blockwise
+    sizes = [1, 129, 8192, 8192 * 3 + 77, 0, 100_003, 8192 * 2, 300]
+    xs = [varied_bf16(n, seed=700 + i) if n else np.zeros(0, np.uint16) for i, n in enumerate(sizes)]
+    dx = [bf16_from_bits(x) if x.size else torch.empty(0, dtype=torch.bfloat16, device="cuda") for x in xs]
+    gc = [Guarded(n, torch.uint8) if n else None for n in sizes]
+    gs = [Guarded((n + 127) // 128, torch.float32) if n else None for n in sizes]
+    codes = [g.t if g else torch.empty(0, dtype=torch.uint8, device="cuda") for g in gc]
+    scales = [g.t if g else torch.empty(1, dtype=torch.float32, device="cuda") for g in gs]
+    w.fp8q_quantize_blockwise_group(dx, fmt, flags, codes=codes, scales=scales)
+    torch.cuda.synchronize()
+    for i, n in enumerate(sizes):
+        if n == 0:
+            continue
+        assert gc[i].intact() and gs[i].intact(), f"item {i} wrote outside its buffers"
+        ec, es = orc.quantize_blockwise(xs[i], fmt)
+        assert_same_f32(gs[i].t.cpu().numpy(), es, f"item {i} scales")
+        assert_same(u8(gc[i].t), ec, f"item {i} codes")

@@ -54,6 +54,15 @@ class fp8q_hop_t(ctypes.Structure):
 
 
 FP8Q_MAX_HOP_GROUP = 16
+
+
+class fp8q_quant_t(ctypes.Structure):
+    """One item of fp8q_quantize_blockwise_group (same layout as the C struct)."""
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("n", ctypes.c_size_t), ("codes", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p)]
+
+
+FP8Q_MAX_QUANT_GROUP = 16
 FP8Q_HOP_LOCAL_READY = 1
 FP8Q_INPUTS_READY = 1
 
@@ -99,6 +108,7 @@ _SIGNATURES = {
     "fp8q_ring_hop_group": ([ctypes.POINTER(fp8q_hop_t), _int, _int, _vp], _int),
     "fp8q_ring_hop_group_ex": ([ctypes.POINTER(fp8q_hop_t), _int, _int, ctypes.c_uint, _vp], _int),
     "fp8q_quantize_blockwise_ex": ([_vp, _sz, _int, _vp, _vp, ctypes.c_uint, _vp], _int),
+    "fp8q_quantize_blockwise_group": ([ctypes.POINTER(fp8q_quant_t), _int, _int, ctypes.c_uint, _vp], _int),
     "fp8q_dequant_reduce_ex": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _vp, ctypes.c_uint,
                                 _vp], _int),
     "mxfp8_quantize_swizzled_group_ex": ([ctypes.POINTER(mxfp8_tensor_t), _int, ctypes.c_uint, _vp], _int),
@@ -217,6 +227,28 @@ def fp8q_quantize_blockwise_ex(x: torch.Tensor, fmt="e4m3", flags: int = 0, code
                                scales: Optional[torch.Tensor] = None, stream=None):
     """fp8q_quantize_blockwise with flags (FP8Q_INPUTS_READY)."""
     return fp8q_quantize_blockwise(x, fmt, codes=codes, scales=scales, stream=stream, flags=flags)
+
+
+def fp8q_quantize_blockwise_group(xs: Sequence[torch.Tensor], fmt="e4m3", flags: int = 0,
+                                  codes: Optional[Sequence[torch.Tensor]] = None,
+                                  scales: Optional[Sequence[torch.Tensor]] = None, stream=None):
+    """Several bf16 arrays quantized blockwise in one launch -> (list of
+    codes, list of scales), as one fp8q_quantize_blockwise per array would give."""
+    count = len(xs)
+    arr = (fp8q_quant_t * max(count, 1))()
+    outc, outs = [], []
+    for i, x in enumerate(xs):
+        n = x.numel()
+        c = codes[i] if codes is not None else torch.empty(n, dtype=torch.uint8, device=x.device)
+        sc = scales[i] if scales is not None else torch.empty(max(fp8q_num_scales(n), 1), dtype=torch.float32,
+                                                              device=x.device)
+        arr[i] = fp8q_quant_t(_dev(x, f"xs[{i}]", torch.bfloat16), n, _dev(c, f"codes[{i}]", torch.uint8, n),
+                              _dev(sc, f"scales[{i}]", torch.float32, fp8q_num_scales(n)))
+        outc.append(c)
+        outs.append(sc)
+    _check("fp8q_quantize_blockwise_group",
+           lib().fp8q_quantize_blockwise_group(arr, count, _fmt(fmt), flags, _stream(stream)))
+    return outc, outs
 
 
 def _ptr_array(ts: Sequence[torch.Tensor], what: str, dtype, numel: int):

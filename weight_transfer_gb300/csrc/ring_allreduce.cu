@@ -8,7 +8,8 @@
 // 2 (P-1)/P of the gradient bytes per GPU: 12.25 GB for 7 GB on 8 GPUs).
 //
 // Schedule (chunk c = elements [c m, (c+1) m), m = n / P):
-//   reduce-scatter  step 0: rank i quantizes its chunk i and sends it on;
+//   reduce-scatter  step 0: rank i quantizes its chunk i and sends it on (the
+//                   P quantizations are one grouped launch);
 //                   step s = 1 .. P-1: rank i makes one ring hop on the
 //                   message from rank i-1 (chunk (i-s) mod P) with its own
 //                   chunk; the P hops of a step are one grouped launch.
@@ -90,13 +91,13 @@ extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, vo
         return static_cast<const uint16_t*>(base) + (size_t)c * m;
     };
 
-    // reduce-scatter, step 0: every rank quantizes its own chunk.  From the
-    // second quantize on, the partials' writer (the caller's work) is at
-    // least two launches back, so the inputs may be copied early.
-    for (int i = 0; i < ranks; ++i) {
-        const fp8q_status_t st = fp8q_quantize_blockwise_ex(chunk(partials[i], i), m, fmt, msg_codes(0, i),
-                                                            msg_scales(0, i), i > 0 ? FP8Q_INPUTS_READY : 0u,
-                                                            stream);
+    // reduce-scatter, step 0: every rank quantizes its own chunk, all ranks
+    // in one launch (the partials may have been written by the caller's last
+    // kernel, so this launch waits for it before reading)
+    {
+        fp8q_quant_t items[FP8Q_MAX_QUANT_GROUP];
+        for (int i = 0; i < ranks; ++i) items[i] = {chunk(partials[i], i), m, msg_codes(0, i), msg_scales(0, i)};
+        const fp8q_status_t st = fp8q_quantize_blockwise_group(items, ranks, fmt, 0u, stream);
         if (st != FP8Q_OK) return st;
     }
     // steps 1 .. P-1: one hop per rank, all ranks in one launch
