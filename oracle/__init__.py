@@ -20,6 +20,9 @@ Parity status of each function (what pins it is in ``tests/test_oracle_*``):
   quantize_tensorwise                pinned (one block: equals the blockwise
                                      quantizer; power-of-two scales vs torch)
   ring_hop_bf16_requant              pinned (equals quantize of the bf16 sum)
+  dequantize_mean                    pinned (the quotient evaluated in float64
+                                     and rounded once; divisor 1 is the plain
+                                     dequantize)
   mxfp8 dequantize / unswizzle       pinned (torch float8 decode times a power
                                      of two; round trip; the hand swizzle table)
   scale swizzle                      formula pinned by a hand table and a
@@ -88,6 +91,7 @@ def lib() -> ctypes.CDLL:
         L.orc_num_blocks.restype = _sz
         L.orc_quantize_blockwise.argtypes = [_u16p, _sz, ctypes.c_int, _u8p, _f32p]
         L.orc_dequantize.argtypes = [_u8p, _f32p, _sz, ctypes.c_int, _u16p, _f32p]
+        L.orc_dequantize_mean.argtypes = [_u8p, _f32p, _sz, ctypes.c_int, ctypes.c_int, _u16p, _f32p]
         L.orc_dequant_reduce.argtypes = [ctypes.POINTER(_u8p), ctypes.POINTER(_f32p), ctypes.c_int, _sz,
                                          ctypes.c_int, _u16p, _f32p]
         L.orc_ring_hop.argtypes = [_u8p, _f32p, _u16p, _sz, ctypes.c_int, _u8p, _f32p, _u16p]
@@ -191,6 +195,19 @@ def dequantize(codes, scales, fmt: int):
     ob = np.empty(n, np.uint16)
     of = np.empty(n, np.float32)
     lib().orc_dequantize(_p(codes, _u8p), _p(scales, _f32p), n, fmt, _p(ob, _u16p), _p(of, _f32p))
+    return ob, of
+
+
+def dequantize_mean(codes, scales, fmt: int, ranks: int):
+    """dequantize, then the binary32 value divided by ``ranks`` (true
+    division) -> (bf16 bits u16[n], f32[n])."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    n = codes.size
+    ob = np.empty(n, np.uint16)
+    of = np.empty(n, np.float32)
+    lib().orc_dequantize_mean(_p(codes, _u8p), _p(scales, _f32p), n, fmt, int(ranks), _p(ob, _u16p),
+                              _p(of, _f32p))
     return ob, of
 
 

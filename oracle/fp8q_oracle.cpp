@@ -235,6 +235,26 @@ void orc_dequantize(const uint8_t* codes, const float* scales, size_t n, int fmt
     }
 }
 
+// ------------------------------------------- dequantize, then a mean ------
+// The all-gather end of the ring AllReduce turned into a mean over the
+// ranks: the data-parallel gradient collective of "How to Speed Up VLA
+// Training Step by Step" (PCIe paragraph) reduces the ranks' gradients, and
+// data-parallel training divides that sum by the number of ranks.  The pages
+// print no formula; the reading taken here divides the decoded binary32 sum
+// once, by true division, then rounds to bf16:
+//   q_i = RN(RN(decode(c_i) * s_b) / ranks);  out_bf16 = RNE_bf16(q_i).
+void orc_dequantize_mean(const uint8_t* codes, const float* scales, size_t n, int fmt, int ranks,
+                         uint16_t* out_bf16, float* out_f32) {
+    const Fmt& F = fmt_of(fmt);
+    const float p = (float)ranks;
+    for (size_t i = 0; i < n; ++i) {
+        float d = decode_f(F, codes[i]) * scales[i / 128];
+        float q = d / p;
+        if (out_f32) out_f32[i] = q;
+        if (out_bf16) out_bf16[i] = f32_to_bf16(q);
+    }
+}
+
 // ------------------------------------------- (b) fused dequant-reduce -----
 // [P1] "FP8 Transmission Optimization and Bottlenecks": k shards are
 // dequantized and summed without writing the dequantized values out.

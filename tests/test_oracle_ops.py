@@ -245,6 +245,45 @@ def test_dequantize_power_of_two(orc):
     assert np.array_equal(of, (torch_fp8_decode(0, c) * np.repeat(s, 128)).astype(np.float32))
 
 
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("ranks", [2, 3, 5, 7, 8, 16])
+def test_dequantize_mean_is_one_true_division(orc, fmt, ranks):
+    # The product decode(c) * s is exact in float64 and the quotient of two
+    # binary32 values rounded to float64 and then to binary32 equals the
+    # single binary32 rounding (53 >= 2*24 + 2; Figueroa 1995).  The scales
+    # span normal and subnormal binary32 quotients; a multiply by RN(1/P)
+    # instead of the division, a division of the bf16 value, or a dropped
+    # divisor each fail here.
+    rng = np.random.default_rng(70 + 10 * fmt + ranks)
+    n = 128 * 48
+    c = rng.integers(0, 256, n, dtype=np.uint8)
+    dec = torch_fp8_decode(fmt, c)
+    c[~np.isfinite(dec)] = 0x21
+    dec = torch_fp8_decode(fmt, c)
+    s = (2.0 ** rng.uniform(-140, 40, n // 128)).astype(np.float32)
+    s[:4] = [0.0, 1.0, 2.0 ** -126, 2.0 ** -149]
+    ob, of = orc.dequantize_mean(c, s, fmt, ranks)
+    d = (dec.astype(np.float64) * np.repeat(s, 128).astype(np.float64)).astype(np.float32)
+    q = (d.astype(np.float64) / ranks).astype(np.float32)
+    assert np.array_equal(of.view(np.uint32), q.view(np.uint32))
+    assert np.array_equal(ob, bf16_bits(q))
+    if ranks == 3:
+        # a hand case: 0x38 (1.0) at s = 1.5 is 1.5, and 1.5 / 3 = 0.5 exactly
+        ob1, of1 = orc.dequantize_mean(np.array([0x38 if fmt == 0 else 0x3C], np.uint8),
+                                       np.array([1.5], np.float32), fmt, 3)
+        assert of1[0] == 0.5 and ob1[0] == 0x3F00
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_dequantize_mean_by_one_is_dequantize(orc, fmt):
+    rng = np.random.default_rng(80 + fmt)
+    c = rng.integers(0, 256, 128 * 9 + 5, dtype=np.uint8)
+    s = (2.0 ** rng.uniform(-100, 30, 10)).astype(np.float32)
+    ob, of = orc.dequantize(c, s, fmt)
+    mb, mf = orc.dequantize_mean(c, s, fmt, 1)
+    assert np.array_equal(ob, mb) and np.array_equal(of.view(np.uint32), mf.view(np.uint32))
+
+
 # ------------------------------------------------------------ ring hop ----
 @pytest.mark.parametrize("fmt", [0, 1])
 def test_ring_hop_zero_local_is_requant_identity(orc, fmt):
