@@ -153,7 +153,7 @@ def measured_peaks():
 def kernel_source_hash(name):
     src = {"mxfp8_quantize_kernel": "mxfp8.cu", "quantize_blockwise_kernel": "quantize.cu",
            "dequant_reduce_kernel": "reduce.cu", "ring_hop_kernel": "ring_hop.cu",
-           "mxfp8_dequantize_kernel": "mxfp8_receive.cu"}[name]
+           "mxfp8_dequantize_kernel": "mxfp8_receive.cu", "gather_decode_kernel": "reduce.cu"}[name]
     h = hashlib.sha256()
     for f in (src, "fp8q_device.cuh"):
         with open(os.path.join(ROOT, "weight_transfer_gb300", "csrc", f), "rb") as fh:
@@ -712,6 +712,19 @@ def run_profile_case(case, launches):
         print(json.dumps({"profile_case": case, "kernel": "mxfp8_dequantize_kernel", "launches": launches,
                           "bytes_per_launch": 3 * b * mm * kk + sb}))
         return
+    if case == "ring_allreduce_sim":
+        # the simulated 8-rank ring AllReduce of the bucket (outside the
+        # step); its last launch is the all-gather decode (gather_decode_kernel)
+        P, n = wl.k, wl.n
+        parts = [wl.sets[0].bucket[r] for r in range(P)]
+        res = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(P)]
+        ws = torch.empty(int(wl.w.lib().fp8q_ring_allreduce_workspace_bytes(P, n)), dtype=torch.uint8, device=dev)
+        for _ in range(max(1, launches)):
+            wl.w.fp8q_ring_allreduce_sim(parts, "e4m3", results=res, workspace=ws, stream=wl.stream)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": case, "kernel": "gather_decode_kernel", "launches": launches,
+                          "bytes_per_launch": n + 4 * nscales(n) + P * 2 * n}))
+        return
     kind, first = PROFILE_CASES[case]
     _, nbytes, _, fn, fargs = wl.launches[first]
     assert wl.launches[first][0] == kind
@@ -880,12 +893,15 @@ def extra_rows(wl, torch, peak):
     out = {}
     wire = [0]
 
-    def ring():
-        wire[0] = w.fp8q_ring_allreduce_sim(parts, "e4m3", results=res, workspace=ws, stream=st)[1]
+    def ring(mean=False):
+        wire[0] = w.fp8q_ring_allreduce_sim(parts, "e4m3", results=res, workspace=ws, stream=st, mean=mean)[1]
     ms = timed(torch, st, ring, flush)
-    kbytes = P * bytes_quantize(m) + (P - 1) * P * bytes_hop(m, False) + P * (n + 4 * nscales(n) + 2 * n)
+    ms_mean = timed(torch, st, lambda: ring(True), flush)
+    # the all-gather decode reads the one shared copy of the gathered codes
+    # once and writes every rank's result
+    kbytes = P * bytes_quantize(m) + (P - 1) * P * bytes_hop(m, False) + (n + 4 * nscales(n) + P * 2 * n)
     out["ring_allreduce_sim"] = {
-        "ranks": P, "elements": n, "ms": round(ms, 4), "kernel_bytes": kbytes,
+        "ranks": P, "elements": n, "ms": round(ms, 4), "ms_mean": round(ms_mean, 4), "kernel_bytes": kbytes,
         "GB/s": round(kbytes / (ms * 1e-3) / 1e9, 1), "wire_bytes_per_rank": wire[0],
         "bf16_ring_bytes_per_rank": 2 * (P - 1) * m * 2,
         "wire_saving_vs_bf16": round(1 - wire[0] / (2 * (P - 1) * m * 2), 6)}
@@ -901,7 +917,7 @@ def extra_rows(wl, torch, peak):
     ms = timed(torch, st, lambda: w.fp8q_ring_allreduce_sim(big, "e4m3", results=bres, workspace=bws, stream=st),
                flush)
     ml = nl_ // P
-    kb2 = P * bytes_quantize(ml) + (P - 1) * P * bytes_hop(ml, False) + P * (nl_ + 4 * nscales(nl_) + 2 * nl_)
+    kb2 = P * bytes_quantize(ml) + (P - 1) * P * bytes_hop(ml, False) + (nl_ + 4 * nscales(nl_) + P * 2 * nl_)
     out["ring_allreduce_sim_256MiB_per_rank"] = {
         "ranks": P, "elements": nl_, "ms": round(ms, 4), "kernel_bytes": kb2,
         "GB/s": round(kb2 / (ms * 1e-3) / 1e9, 1), "frac_of_peak": round(kb2 / (ms * 1e-3) / 1e9 / peak, 4)}
@@ -1150,7 +1166,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-vec3p5b", action="store_true", help="skip the 3.5e9-element vector row")
-    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES) + ["mxfp8_dequantize"],
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES) + ["mxfp8_dequantize", "ring_allreduce_sim"],
                     help="launch one kernel of the step a few times on its bench inputs and exit (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()

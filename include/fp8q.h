@@ -199,7 +199,9 @@ fp8q_status_t fp8q_ring_hop_group_ex(const fp8q_hop_t* hops, int count, fp8q_for
  *     rank i ends with chunk (i+1) mod P summed over all ranks, as codes;
  *   all-gather: the reduced codes and scales travel unchanged, and every
  *     rank dequantizes the whole vector into results[r] (all ranks equal).
- * A sum, not a mean.
+ *     The ranks share one GPU, so the gathered codes are one buffer: a
+ *     single launch decodes it and writes all P results.
+ * A sum; fp8q_ring_allreduce_sim_ex with FP8Q_ALLREDUCE_MEAN gives the mean.
  *   partials, results : HOST arrays of `ranks` device pointers to n bf16;
  *                       results[r] may be partials[r] (in place)
  *   ranks             : 2 .. FP8Q_MAX_HOP_GROUP (FP8Q_ERR_K otherwise)
@@ -212,6 +214,20 @@ size_t fp8q_ring_allreduce_workspace_bytes(int ranks, size_t n);
 fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, void* const* results, int ranks, size_t n,
                                       fp8q_format_t fmt, void* workspace, size_t workspace_bytes,
                                       uint64_t* wire_bytes, fp8q_stream_t stream);
+
+/* fp8q_ring_allreduce_sim with flags (0 = the sum, as above).
+ * FP8Q_ALLREDUCE_MEAN: the all-gather decode divides each decoded value by
+ * the rank count before the bf16 rounding,
+ *     results[r][i] = RNE_bf16(RN(RN(decode(c_i) * s_b) / ranks))
+ * with a true (correctly rounded) binary32 division; the codes on the wire
+ * and wire_bytes are unchanged.  The pages reduce gradients over the ranks
+ * without printing a mean; data-parallel training averages them, and this
+ * is that average taken once, at the end, on the decoded sum.
+ * Other flag bits: FP8Q_ERR_FLAGS. */
+#define FP8Q_ALLREDUCE_MEAN 1u
+fp8q_status_t fp8q_ring_allreduce_sim_ex(const void* const* partials, void* const* results, int ranks, size_t n,
+                                         fp8q_format_t fmt, void* workspace, size_t workspace_bytes,
+                                         uint64_t* wire_bytes, unsigned int flags, fp8q_stream_t stream);
 
 /* ------------------------------------------------------------ variants ----
  * fp8q_quantize_tensorwise: one scale for the whole tensor (the tensorwise

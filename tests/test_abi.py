@@ -251,3 +251,11 @@ def test_ring_group_and_allreduce_validation(L):
     assert r(pp, rp, 2, 1000, 0, A + 40 * MB, 1 << 20, None, None) == ERR_SIZE
     assert r(pp, rp, 2, 1024, 0, A + 40 * MB, 16, None, None) == ERR_SIZE       # workspace too small
     assert r(pp, rp, 2, 0, 0, None, 0, None, None) == OK
+    rx = L.fp8q_ring_allreduce_sim_ex
+    assert rx(pp, rp, 2, 1024, 0, A + 40 * MB, 1 << 20, None, 2, None) == ERR_FLAGS      # unknown flag bit
+    assert rx(pp, rp, 2, 1024, 9, A + 40 * MB, 1 << 20, None, w.FP8Q_ALLREDUCE_MEAN, None) == ERR_FORMAT
+    assert rx(pp, rp, 1, 1024, 0, A + 40 * MB, 1 << 20, None, w.FP8Q_ALLREDUCE_MEAN, None) == ERR_K
+    assert rx(pp, rp, 2, 0, 0, None, 0, None, w.FP8Q_ALLREDUCE_MEAN, None) == OK
+    # results of two ranks in one place
+    same = (ctypes.c_void_p * 2)(A + 20 * MB, A + 20 * MB)
+    assert rx(pp, same, 2, 1024, 0, A + 40 * MB, 1 << 20, None, w.FP8Q_ALLREDUCE_MEAN, None) == ERR_ALIAS

@@ -46,7 +46,7 @@ def test_hop_group_equals_single_hops(w, orc, fmt):
             assert_same(bits16(ob), e[2], f"hop {i} bf16")
 
 
-def oracle_allreduce(orc, parts, fmt):
+def oracle_allreduce(orc, parts, fmt, mean=False):
     """The same ring schedule, step by step, on the oracle."""
     P = len(parts)
     n = parts[0].size
@@ -66,21 +66,49 @@ def oracle_allreduce(orc, parts, fmt):
         msgs = new
     codes = np.concatenate([f[0] for f in final])
     scales = np.concatenate([f[1] for f in final])
-    ob, _ = orc.dequantize(codes, scales, fmt)
+    ob, _ = orc.dequantize_mean(codes, scales, fmt, P) if mean else orc.dequantize(codes, scales, fmt)
     return ob
 
 
+@pytest.mark.parametrize("mean", [False, True])
 @pytest.mark.parametrize("fmt", [0, 1])
-@pytest.mark.parametrize("P,n", [(2, 1024), (3, 3 * 512 * 7), (8, 8 * 512 * 33), (16, 16 * 512 * 3)])
-def test_ring_allreduce_matches_oracle_schedule(w, orc, fmt, P, n):
+@pytest.mark.parametrize("P,n", [(2, 1024), (3, 3 * 512 * 7), (5, 5 * 512 * 11), (8, 8 * 512 * 33),
+                                 (16, 16 * 512 * 3)])
+def test_ring_allreduce_matches_oracle_schedule(w, orc, fmt, P, n, mean):
+    # n = 3 * 512 * 7 and 5 * 512 * 11 end in a ragged 4096-element tile of
+    # the all-gather decode; P = 3, 5 make the mean a rounded division
     parts = [bits16(gen.ring_partial(r, n)) for r in range(P)]
-    res, wire = w.fp8q_ring_allreduce_sim([bf16_from_bits(p) for p in parts], fmt)
+    res, wire = w.fp8q_ring_allreduce_sim([bf16_from_bits(p) for p in parts], fmt, mean=mean)
     torch.cuda.synchronize()
-    want = oracle_allreduce(orc, parts, fmt)
+    want = oracle_allreduce(orc, parts, fmt, mean)
     for r in range(P):
         assert_same(bits16(res[r]), want, f"rank {r}")
     m = n // P
     assert wire == 2 * (P - 1) * (m + 4 * (m // 128))
+
+
+@pytest.mark.parametrize("P,n", [(8, 8 * 512 * 33), (3, 3 * 512 * 7)])
+def test_ring_allreduce_in_place_mean(w, orc, P, n):
+    # results written over the partials (each rank's own), with the mean
+    parts = [bits16(gen.ring_partial(r, n)) for r in range(P)]
+    dev = [bf16_from_bits(p) for p in parts]
+    res, _ = w.fp8q_ring_allreduce_sim(dev, 0, results=dev, mean=True)
+    torch.cuda.synchronize()
+    want = oracle_allreduce(orc, parts, 0, True)
+    for r in range(P):
+        assert res[r].data_ptr() == dev[r].data_ptr()
+        assert_same(bits16(res[r]), want, f"rank {r}")
+
+
+def test_ring_allreduce_ddp_bucket_mean(w, orc):
+    # the 8-rank bucket at full size, averaged: every rank equals the oracle
+    P, n = gen.DDP_K, gen.DDP_N
+    parts = [bits16(gen.ddp_shard(r)) for r in range(P)]
+    res, _ = w.fp8q_ring_allreduce_sim([bf16_from_bits(p) for p in parts], "e4m3", mean=True)
+    torch.cuda.synchronize()
+    want = oracle_allreduce(orc, parts, 0, True)
+    for r in range(P):
+        assert_same(bits16(res[r]), want, f"rank {r}")
 
 
 def test_ring_allreduce_ddp_bucket_wire_bytes_and_accuracy(w, orc):

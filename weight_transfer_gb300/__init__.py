@@ -65,6 +65,7 @@ class fp8q_quant_t(ctypes.Structure):
 FP8Q_MAX_QUANT_GROUP = 16
 FP8Q_HOP_LOCAL_READY = 1
 FP8Q_INPUTS_READY = 1
+FP8Q_ALLREDUCE_MEAN = 1
 
 
 class mxfp8_tensor_t(ctypes.Structure):
@@ -115,6 +116,8 @@ _SIGNATURES = {
     "fp8q_ring_allreduce_workspace_bytes": ([_int, _sz], _sz),
     "fp8q_ring_allreduce_sim": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _sz,
                                  ctypes.POINTER(ctypes.c_uint64), _vp], _int),
+    "fp8q_ring_allreduce_sim_ex": ([ctypes.POINTER(_vp), ctypes.POINTER(_vp), _int, _sz, _int, _vp, _sz,
+                                    ctypes.POINTER(ctypes.c_uint64), ctypes.c_uint, _vp], _int),
     "fp8q_num_scales": ([_sz], _sz),
     "mxfp8_swizzled_scale_bytes": ([_i64, _i64, _i64], _sz),
     "fp8q_status_string": ([_int], ctypes.c_char_p),
@@ -374,9 +377,10 @@ def fp8q_ring_hop_group_ex(hops: Sequence[dict], fmt="e4m3", flags: int = 0, str
 
 
 def fp8q_ring_allreduce_sim(partials: Sequence[torch.Tensor], fmt="e4m3", results: Optional[Sequence[torch.Tensor]] = None,
-                            workspace: Optional[torch.Tensor] = None, stream=None):
+                            workspace: Optional[torch.Tensor] = None, stream=None, mean: bool = False):
     """Ring AllReduce of P ranks' bf16 vectors held on one GPU, over the FP8
-    wire format -> (list of P result tensors, wire bytes sent per rank)."""
+    wire format -> (list of P result tensors, wire bytes sent per rank).
+    mean=True divides the decoded sum by P (FP8Q_ALLREDUCE_MEAN)."""
     P = len(partials)
     n = partials[0].numel()
     dev = partials[0].device
@@ -388,9 +392,10 @@ def fp8q_ring_allreduce_sim(partials: Sequence[torch.Tensor], fmt="e4m3", result
     pp = (_vp * P)(*[_dev(t, f"partials[{i}]", torch.bfloat16, n) for i, t in enumerate(partials)])
     rp = (_vp * P)(*[_dev(t, f"results[{i}]", torch.bfloat16, n) for i, t in enumerate(results)])
     wire = ctypes.c_uint64(0)
-    st = lib().fp8q_ring_allreduce_sim(pp, rp, P, n, _fmt(fmt), _dev(workspace, "workspace", torch.uint8),
-                                       workspace.numel(), ctypes.byref(wire), _stream(stream))
-    _check("fp8q_ring_allreduce_sim", st)
+    flags = FP8Q_ALLREDUCE_MEAN if mean else 0
+    st = lib().fp8q_ring_allreduce_sim_ex(pp, rp, P, n, _fmt(fmt), _dev(workspace, "workspace", torch.uint8),
+                                          workspace.numel(), ctypes.byref(wire), flags, _stream(stream))
+    _check("fp8q_ring_allreduce_sim_ex", st)
     return list(results), int(wire.value)
 
 

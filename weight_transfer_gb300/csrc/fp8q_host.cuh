@@ -90,10 +90,12 @@ inline unsigned grid_for(size_t work_blocks, int resident) {
     return (unsigned)(g > 0 ? g : 1);
 }
 
-// fp8q_dequantize with flags (FP8Q_INPUTS_READY), for the library's own
-// schedules (the simulated ring AllReduce).
-fp8q_status_t dequantize_entry(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
-                               void* out_bf16, float* out_fp32, unsigned flags, fp8q_stream_t stream);
+// The all-gather decode of the simulated ring AllReduce: n codes and their
+// scales decoded once, the bf16 values written to each of the `count`
+// outputs (count <= FP8Q_MAX_HOP_GROUP); with mean_divisor > 0 each decoded
+// value is divided by it (true division) before the bf16 rounding.
+fp8q_status_t gather_decode_entry(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                                  void* const* outs, int count, int mean_divisor, fp8q_stream_t stream);
 
 // Process-wide switch of programmatic dependent launch (fp8q_set_launch_overlap).
 bool launch_overlap();

@@ -349,10 +349,8 @@ extern "C" fp8q_status_t fp8q_dequant_reduce_ex(const uint8_t* const* codes, con
     return reduce_entry(codes, scales, k, n, fmt, out_bf16, out_fp32, flags, stream);
 }
 
-namespace fp8q {
-fp8q_status_t dequantize_entry(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
-                               void* out_bf16, float* out_fp32, unsigned flags, fp8q_stream_t stream) {
-    if (flags & ~FP8Q_INPUTS_READY) return FP8Q_ERR_FLAGS;
+extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                                         void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
     ShardPtrs sh;
     const uint8_t* c[1] = {codes};
     const float* sc[1] = {scales};
@@ -360,16 +358,168 @@ fp8q_status_t dequantize_entry(const uint8_t* codes, const float* scales, size_t
     if (st != FP8Q_OK || n == 0) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint16_t* ob = static_cast<uint16_t*>(out_bf16);
-    const int ready = (flags & FP8Q_INPUTS_READY) ? 1 : 0;
-    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(sh, 1, n, ob, out_fp32, s, ready)
-                            : launch_reduce<kE5M2, false>(sh, 1, n, ob, out_fp32, s, ready);
+    return fmt == FP8Q_E4M3 ? launch_reduce<kE4M3, false>(sh, 1, n, ob, out_fp32, s)
+                            : launch_reduce<kE5M2, false>(sh, 1, n, ob, out_fp32, s);
+}
+
+namespace fp8q {
+
+
+// ------------------------------------------------ all-gather decode ----
+// The end of the simulated ring AllReduce: every rank decodes the same
+// gathered codes.  The ranks share one GPU and one copy of the codes, so a
+// tile of 4096 codes and its 32 scales is staged once (bulk copies, like the
+// reduce with k = 1) and its bf16 values are stored to every rank's output.
+// Each of the 512 threads takes 8 consecutive elements (one 16-byte store
+// per output; a warp writes 512 contiguous bytes of each output).
+// MEAN: the decoded value is divided by `divisor` (the rank count) first,
+// RN(d / divisor), by markstein_div<2> from y = RN(1/divisor) (exact for
+// binary32 dividends with |d| >= 2^-78) and by the IEEE division below that.
+
+constexpr int kGatherStages = 4;
+constexpr uint32_t kGatherStageBytes = kRedTile + 4 * (kRedTile / 128);
+constexpr size_t kGatherSmem = (size_t)kGatherStages * kGatherStageBytes + 8 * kGatherStages;
+
+struct GatherDests {
+    uint16_t* out[FP8Q_MAX_HOP_GROUP];
+};
+
+template <bool MEAN>
+__device__ __forceinline__ float gather_value(float d, float divisor, float y) {
+    if (!MEAN) return d;
+    return fabsf(d) >= 0x1p-78f ? markstein_div<2>(d, divisor, y) : __fdiv_rn(d, divisor);
+}
+
+template <int FMT, bool MEAN>
+__global__ void __launch_bounds__(kRedThreads)
+gather_decode_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales, size_t n,
+                     const __grid_constant__ GatherDests dst, int count, float divisor) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGatherStages * kGatherStageBytes);
+    const size_t ntiles = (n + kRedTile - 1) / kRedTile;
+    const size_t nstaged = n / kRedTile;
+    const unsigned tid = threadIdx.x;
+    const float y = MEAN ? __frcp_rn(divisor) : 1.0f;
+
+    if (tid == 0) {
+        for (int s = 0; s < kGatherStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    auto issue = [&](size_t t, int s) {           // thread 0 only
+        uint8_t* st = smem + (size_t)s * kGatherStageBytes;
+        mbar_arrive_expect_tx(&full[s], kGatherStageBytes);
+        bulk_g2s(st, codes + t * kRedTile, kRedTile, &full[s]);
+        bulk_g2s(st + kRedTile, scales + t * (kRedTile / 128), 4 * kRedTile / 128, &full[s]);
+    };
+    // the codes are the previous launch's output: no copy before the wait
+    dependency_wait();
+    allow_dependents();
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < kGatherStages; ++s) {
+            const size_t t = blockIdx.x + (size_t)s * gridDim.x;
+            if (t < nstaged) issue(t, s);
+        }
+    }
+
+    int it = 0;
+    bool failed = false;
+    for (size_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int s = it % kGatherStages;
+        const bool staged = t < nstaged;
+        const bool ok = staged ? mbar_wait(&full[s], (uint32_t)(it / kGatherStages) & 1u) : true;
+        const uint32_t el = 8 * tid;
+        const size_t e = t * kRedTile + el;
+        if (staged) {
+            const uint8_t* st = smem + (size_t)s * kGatherStageBytes;
+            const uint2 c8 = *reinterpret_cast<const uint2*>(st + el);
+            const float sc = *reinterpret_cast<const float*>(st + kRedTile + (el >> 7) * 4);
+            float d[8];
+            decode_fp8x4<FMT>(c8.x, d);
+            decode_fp8x4<FMT>(c8.y, d + 4);
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                w[q] = pack_bf16x2(gather_value<MEAN>(__fmul_rn(d[2 * q], sc), divisor, y),
+                                   gather_value<MEAN>(__fmul_rn(d[2 * q + 1], sc), divisor, y));
+            const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int o = 0; o < FP8Q_MAX_HOP_GROUP; ++o)
+                if (o < count) st_stream(dst.out[o] + e, v);
+        } else if (e < n) {
+            // the ragged last tile, element by element from global memory
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            for (int q = 0; q < 8; ++q) {
+                if (e + q < n) {
+                    const float dq = decode_fp8x2<FMT>(codes[e + q]).x;
+                    const float v = gather_value<MEAN>(__fmul_rn(dq, scales[(e + q) >> 7]), divisor, y);
+                    w[q >> 1] |= (pack_bf16x2(v, 0.0f) & 0xFFFFu) << ((q & 1) * 16);
+                }
+            }
+            for (int o = 0; o < count; ++o) st_u16_tail(dst.out[o] + e, w, 4, (long long)n - (long long)e);
+        }
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0) {
+            const size_t tn = t + (size_t)kGatherStages * gridDim.x;
+            if (tn < nstaged) {
+                fence_proxy_async_smem();
+                issue(tn, s);
+            }
+        }
+    }
+    if (failed && tid == 0) {
+        raise_error(kErrCopyTimeout);
+        for (int j = it; j < it + kGatherStages; ++j) {
+            const size_t tj = blockIdx.x + (size_t)j * gridDim.x;
+            if (tj < nstaged) mbar_wait(&full[j % kGatherStages], (uint32_t)(j / kGatherStages) & 1u);
+        }
+    }
+}
+
+template <int FMT, bool MEAN>
+static fp8q_status_t launch_gather(const uint8_t* codes, const float* scales, size_t n, const GatherDests& dst,
+                                   int count, float divisor, cudaStream_t s) {
+    auto kernel = gather_decode_kernel<FMT, MEAN>;
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc, kernel, kRedThreads, kGatherSmem, 0, &resident);
+    if (st != FP8Q_OK) return st;
+    const unsigned grid = grid_for((n + kRedTile - 1) / kRedTile, resident);
+    return launch(kernel, grid, kRedThreads, kGatherSmem, s, codes, scales, n, dst, count, divisor);
+}
+
+fp8q_status_t gather_decode_entry(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                                  void* const* outs, int count, int mean_divisor, fp8q_stream_t stream) {
+    if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
+    if (count < 1 || count > FP8Q_MAX_HOP_GROUP || mean_divisor < 0 || mean_divisor > FP8Q_MAX_HOP_GROUP)
+        return FP8Q_ERR_K;
+    if (n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
+    if (n == 0) return FP8Q_OK;
+    if (!codes || !scales || !outs) return FP8Q_ERR_NULL;
+    if (!aligned16(codes) || !aligned16(scales)) return FP8Q_ERR_ALIGN;
+    const size_t nb = fp8q_num_scales(n);
+    GatherDests dst = {};
+    for (int o = 0; o < count; ++o) {
+        if (!outs[o]) return FP8Q_ERR_NULL;
+        if (!aligned16(outs[o])) return FP8Q_ERR_ALIGN;
+        if (overlaps(outs[o], 2 * n, codes, n) || overlaps(outs[o], 2 * n, scales, 4 * nb)) return FP8Q_ERR_ALIAS;
+        for (int q = 0; q < o; ++q)
+            if (overlaps(outs[o], 2 * n, outs[q], 2 * n)) return FP8Q_ERR_ALIAS;
+        dst.out[o] = static_cast<uint16_t*>(outs[o]);
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float div = (float)(mean_divisor > 0 ? mean_divisor : 1);
+    if (fmt == FP8Q_E4M3)
+        return mean_divisor > 0 ? launch_gather<kE4M3, true>(codes, scales, n, dst, count, div, s)
+                                : launch_gather<kE4M3, false>(codes, scales, n, dst, count, div, s);
+    return mean_divisor > 0 ? launch_gather<kE5M2, true>(codes, scales, n, dst, count, div, s)
+                            : launch_gather<kE5M2, false>(codes, scales, n, dst, count, div, s);
 }
 }  // namespace fp8q
 
-extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
-                                         void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
-    return dequantize_entry(codes, scales, n, fmt, out_bf16, out_fp32, 0, stream);
-}
 
 extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const float* const* scales,
                                                      int k, size_t n, fp8q_format_t fmt, float* workspace,

@@ -17,9 +17,12 @@
 //                   over all ranks, as codes and scales.
 //   all-gather      the P reduced chunks travel the ring unchanged (codes and
 //                   scales are the wire format); every rank dequantizes all
-//                   of them, so every rank ends with the same bf16 vector.
+//                   of them, so every rank ends with the same bf16 vector
+//                   (optionally divided by P: the mean).
 // On one GPU the "send" is the next rank reading the sender's buffer; the
-// bytes that would cross the wire are counted and returned.
+// bytes that would cross the wire are counted and returned.  The gathered
+// codes are then one buffer that every rank reads, so the all-gather decode
+// is one launch that decodes each tile once and writes all P results.
 #include "fp8q_host.cuh"
 
 namespace {
@@ -51,11 +54,12 @@ extern "C" size_t fp8q_ring_allreduce_workspace_bytes(int ranks, size_t n) {
     return layout_of(ranks, n).total;
 }
 
-extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, void* const* results, int ranks,
-                                                 size_t n, fp8q_format_t fmt, void* workspace,
-                                                 size_t workspace_bytes, uint64_t* wire_bytes,
-                                                 fp8q_stream_t stream) {
+extern "C" fp8q_status_t fp8q_ring_allreduce_sim_ex(const void* const* partials, void* const* results, int ranks,
+                                                    size_t n, fp8q_format_t fmt, void* workspace,
+                                                    size_t workspace_bytes, uint64_t* wire_bytes, unsigned int flags,
+                                                    fp8q_stream_t stream) {
     using namespace fp8q;
+    if (flags & ~FP8Q_ALLREDUCE_MEAN) return FP8Q_ERR_FLAGS;
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
     if (ranks < 2 || ranks > FP8Q_MAX_HOP_GROUP) return FP8Q_ERR_K;
     if (n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
@@ -127,14 +131,21 @@ extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, vo
         const fp8q_status_t st = fp8q_ring_hop_group_ex(hops, ranks, fmt, FP8Q_HOP_LOCAL_READY, stream);
         if (st != FP8Q_OK) return st;
     }
-    // all-gather of the reduced codes, then every rank decodes the whole vector
-    // (the last hop group wrote the reduced codes; from the second dequantize
-    // on it is at least two launches back)
-    for (int r = 0; r < ranks; ++r) {
-        const fp8q_status_t st = dequantize_entry(fin_codes, fin_scales, n, fmt, results[r], nullptr,
-                                                  r > 0 ? FP8Q_INPUTS_READY : 0u, stream);
+    // all-gather of the reduced codes, then every rank decodes the whole
+    // vector: one launch writes all P results
+    {
+        const int divisor = (flags & FP8Q_ALLREDUCE_MEAN) ? ranks : 0;
+        const fp8q_status_t st = gather_decode_entry(fin_codes, fin_scales, n, fmt, results, ranks, divisor, stream);
         if (st != FP8Q_OK) return st;
     }
     if (wire_bytes) *wire_bytes = 2ull * (uint64_t)(ranks - 1) * (uint64_t)(m + 4 * (m / 128));
     return FP8Q_OK;
+}
+
+extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, void* const* results, int ranks,
+                                                 size_t n, fp8q_format_t fmt, void* workspace,
+                                                 size_t workspace_bytes, uint64_t* wire_bytes,
+                                                 fp8q_stream_t stream) {
+    return fp8q_ring_allreduce_sim_ex(partials, results, ranks, n, fmt, workspace, workspace_bytes, wire_bytes, 0u,
+                                      stream);
 }
