@@ -152,6 +152,20 @@ def test_mxfp8_dequantize_and_unswizzle(w, orc, b, m, k):
         assert_same(u8(plain).ravel(), orc.mxfp8_unswizzle(ss, b, m, k), "row-major scales")
 
 
+@pytest.mark.parametrize("b,m,k", [(30, 200, 4000), (40, 768, 2048)])
+def test_mxfp8_dequantize_many_tiles_per_cta(w, orc, b, m, k):
+    # more tiles than three per CTA, so every shared-memory stage is refilled;
+    # (30, 200, 4000): rows past each matrix's end and a partial column tile
+    rng = np.random.default_rng(m + k)
+    codes = rng.integers(0, 256, b * m * k, dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3A
+    sb = w.mxfp8_swizzled_scale_bytes(b, m, k)
+    sc = rng.integers(100, 140, sb, dtype=np.uint8)
+    out = w.mxfp8_dequantize_swizzled(torch.from_numpy(codes.reshape(b, m, k)).cuda(), torch.from_numpy(sc).cuda())
+    torch.cuda.synchronize()
+    assert_same(bits16(out).ravel(), orc.mxfp8_dequantize(codes, sc, b, m, k), "dequantized weights")
+
+
 def test_count_mismatches(w, orc):
     rng = np.random.default_rng(5)
     for n in (1, 15, 16, 17, 4096 + 7, 3_000_001):
