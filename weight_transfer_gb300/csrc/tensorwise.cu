@@ -15,8 +15,18 @@
 
 namespace fp8q {
 
+// Largest bf16 magnitude bits among the 8 elements of v.
+__device__ __forceinline__ uint32_t amax_bits8(const uint4& v, uint32_t m) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
+    return m;
+}
+
 // scale_amax[1] accumulates the amax as binary32 bits (non-negative floats
-// order like their bit patterns).
+// order like their bit patterns).  Each thread keeps four 16-byte loads in
+// flight: with one, the loads a GPU can hold in flight do not cover HBM's
+// latency at full bandwidth.
 __global__ void __launch_bounds__(256)
 tensor_amax_kernel(const uint16_t* __restrict__ x, size_t n, float* scale_amax) {
     dependency_wait();
@@ -25,12 +35,15 @@ tensor_amax_kernel(const uint16_t* __restrict__ x, size_t n, float* scale_amax) 
     const size_t n8 = n / 8;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (size_t i = t0; i < n8; i += stride) {
-        const uint4 v = ld_stream(x + 8 * i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
+    size_t i = t0;
+    for (; i + 3 * stride < n8; i += 4 * stride) {
+        const uint4 v0 = ld_stream(x + 8 * i);
+        const uint4 v1 = ld_stream(x + 8 * (i + stride));
+        const uint4 v2 = ld_stream(x + 8 * (i + 2 * stride));
+        const uint4 v3 = ld_stream(x + 8 * (i + 3 * stride));
+        m = amax_bits8(v3, amax_bits8(v2, amax_bits8(v1, amax_bits8(v0, m))));
     }
+    for (; i < n8; i += stride) m = amax_bits8(ld_stream(x + 8 * i), m);
     for (size_t i = 8 * n8 + t0; i < n; i += stride) m = max(m, (uint32_t)(x[i] & 0x7FFFu));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -47,13 +60,20 @@ tensor_encode_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __restri
     const size_t n8 = n / 8;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (size_t i = t0; i < n8; i += stride) {
-        const uint4 v = ld_stream(x + 8 * i);
+    auto encode8 = [&](const uint4& v, size_t i) {
         float f[8], q[8];
         unpack8(v, f);
         block_quotients<1, 8>(f, s, q);
         st_stream(codes + 8 * i, make_uint2(cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])));
+    };
+    size_t i = t0;
+    for (; i + stride < n8; i += 2 * stride) {     // two loads in flight per thread
+        const uint4 v0 = ld_stream(x + 8 * i);
+        const uint4 v1 = ld_stream(x + 8 * (i + stride));
+        encode8(v0, i);
+        encode8(v1, i + stride);
     }
+    for (; i < n8; i += stride) encode8(ld_stream(x + 8 * i), i);
     for (size_t i = 8 * n8 + t0; i < n; i += stride) {
         float f[1] = {__uint_as_float((uint32_t)x[i] << 16)}, q[1];
         block_quotients<1, 1>(f, s, q);
