@@ -26,8 +26,11 @@ __device__ __forceinline__ int64_t swizzle_offset(int64_t bt, int64_t r, int64_t
 // Dequantize by whole 128 x 128 tiles of the [batch * m, k] code matrix: the
 // tiles of the swizzled scale layout, so tile t's 512 E8M0 bytes are the
 // contiguous bytes [512 t, 512 t + 512) of the scale buffer.  256 threads
-// per tile: 8 per row, 16 codes each (one 16-byte load, two 16-byte bf16
-// stores), 32 rows per pass, 4 passes.  The tile index is split into
+// per tile: 8 per row, 32 rows per pass, 4 passes.  Thread c of a row takes
+// codes [8c, 8c + 8) and [64 + 8c, 64 + 8c + 8) (two 8-byte loads, two
+// 16-byte bf16 stores), so that each store instruction of a warp writes
+// whole 128-byte runs; with 16 consecutive codes per thread a store covered
+// only half of each 32-byte sector it touched.  The tile index is split into
 // (matrix, row tile, column tile) once per tile, in 32-bit arithmetic (the
 // entry point rejects tensors of 2^32 tiles or more).
 __global__ void __launch_bounds__(256)
@@ -37,16 +40,17 @@ mxfp8_dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __rest
     dependency_wait();
     allow_dependents();
     const unsigned tid = threadIdx.x;
-    const unsigned chunk = tid & 7u;               // 16-code chunk inside the tile row
+    const unsigned chunk = tid & 7u;               // codes [8 chunk, +8) and [64 + 8 chunk, +8) of the tile row
     const unsigned rsub = tid >> 3;                // row inside a 32-row pass
-    const unsigned j = chunk >> 1;                 // scale column inside the tile (32 codes)
+    const unsigned j = chunk >> 2;                 // scale column of the first 8 codes; the second's is j + 2
     for (uint32_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
         const uint32_t bt = t / tiles_per_mat;
         const uint32_t rem = t - bt * tiles_per_mat;
         const uint32_t rt = rem / col_tiles;
         const uint32_t ct = rem - rt * col_tiles;
-        const int64_t col = (int64_t)ct * 128 + chunk * 16;
-        if (col >= k) continue;                    // k % 32 == 0: a chunk is wholly in or out
+        const int64_t col = (int64_t)ct * 128 + chunk * 8;
+        if (col >= k) continue;                    // k % 32 == 0: both 8-code runs are in, or the first only, or none
+        const bool second = col + 64 < k;
         const uint8_t* stile = scales + (size_t)t * 512;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
@@ -54,21 +58,27 @@ mxfp8_dequantize_kernel(const uint8_t* __restrict__ codes, const uint8_t* __rest
             const int64_t row = (int64_t)rt * 128 + r;
             if (row >= m) break;                   // later passes are further down
             const size_t e0 = (size_t)((int64_t)bt * m + row) * (size_t)k + (size_t)col;
-            const uint32_t e8 = __ldg(stile + (r & 31u) * 16 + (r >> 5) * 4 + j);
+            const unsigned sb = (r & 31u) * 16 + (r >> 5) * 4;
+            const uint32_t e8a = __ldg(stile + sb + j);
+            const uint32_t e8b = second ? __ldg(stile + sb + j + 2) : 0u;
             // 2^(e8 - 127): a normal binary32 for e8 >= 1, the subnormal 2^-127 for e8 == 0
-            const float factor = __uint_as_float(e8 ? (e8 << 23) : 0x00400000u);
-            const uint4 c = ld_stream(codes + e0);
+            const float fa = __uint_as_float(e8a ? (e8a << 23) : 0x00400000u);
+            const float fb = __uint_as_float(e8b ? (e8b << 23) : 0x00400000u);
+            const uint2 ca = ld_stream8(codes + e0);
+            const uint2 cb = second ? ld_stream8(codes + e0 + 64) : make_uint2(0u, 0u);
             float d[16];
-            decode_fp8x4<kE4M3>(c.x, d);
-            decode_fp8x4<kE4M3>(c.y, d + 4);
-            decode_fp8x4<kE4M3>(c.z, d + 8);
-            decode_fp8x4<kE4M3>(c.w, d + 12);
+            decode_fp8x4<kE4M3>(ca.x, d);
+            decode_fp8x4<kE4M3>(ca.y, d + 4);
+            decode_fp8x4<kE4M3>(cb.x, d + 8);
+            decode_fp8x4<kE4M3>(cb.y, d + 12);
             uint32_t h[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)     // the products are exact; only the bf16 rounding rounds
-                h[i] = pack_bf16x2(__fmul_rn(d[2 * i], factor), __fmul_rn(d[2 * i + 1], factor));
+            for (int i = 0; i < 4; ++i) {   // the products are exact; only the bf16 rounding rounds
+                h[i] = pack_bf16x2(__fmul_rn(d[2 * i], fa), __fmul_rn(d[2 * i + 1], fa));
+                h[4 + i] = pack_bf16x2(__fmul_rn(d[8 + 2 * i], fb), __fmul_rn(d[8 + 2 * i + 1], fb));
+            }
             st_stream(out + e0, make_uint4(h[0], h[1], h[2], h[3]));
-            st_stream(out + e0 + 8, make_uint4(h[4], h[5], h[6], h[7]));
+            if (second) st_stream(out + e0 + 64, make_uint4(h[4], h[5], h[6], h[7]));
         }
     }
 }
