@@ -48,8 +48,19 @@ __global__ void __launch_bounds__(256) copy_segments_kernel(const __grid_constan
         const uint8_t* src = tab.src[s] + off;
         uint8_t* dst = tab.dst[s] + off;
         const uint64_t n16 = len / 16;
-        for (uint64_t i = threadIdx.x; i < n16; i += blockDim.x)
-            st_stream(dst + 16 * i, ld_stream(src + 16 * i));
+        const uint64_t b = blockDim.x;
+        uint64_t i = threadIdx.x;
+        for (; i + 3 * b < n16; i += 4 * b) {          // four loads in flight per thread
+            const uint4 v0 = ld_stream(src + 16 * i);
+            const uint4 v1 = ld_stream(src + 16 * (i + b));
+            const uint4 v2 = ld_stream(src + 16 * (i + 2 * b));
+            const uint4 v3 = ld_stream(src + 16 * (i + 3 * b));
+            st_stream(dst + 16 * i, v0);
+            st_stream(dst + 16 * (i + b), v1);
+            st_stream(dst + 16 * (i + 2 * b), v2);
+            st_stream(dst + 16 * (i + 3 * b), v3);
+        }
+        for (; i < n16; i += b) st_stream(dst + 16 * i, ld_stream(src + 16 * i));
         for (uint64_t i = 16 * n16 + threadIdx.x; i < len; i += blockDim.x) dst[i] = src[i];
     }
 }
