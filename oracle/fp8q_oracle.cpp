@@ -27,7 +27,7 @@
 //       X = floor(log2(amax)) - emax_elem.
 //
 // The pages print no formula or code for any of these steps.  The readings
-// taken where they are silent are these (numbered O1..O17):
+// taken where they are silent are these (numbered O1..O19):
 //  O1 block of 128 elements with one fp32 scale (the only reading that gives
 //     P1's 48.4% byte saving exactly);
 //  O2/O3 s = RN(amax / Fmax); code = RNE_fp8(RN_fp32(x / s)), a true IEEE
@@ -46,6 +46,8 @@
 //     pinned by a hand table and a bijection check, but the choice of this
 //     layout is parity unpinned: nothing on the pages fixes it.
 //  O17 K % 32 != 0 is rejected; K == 32 keeps its one real scale column.
+//  O19 the ring AllReduce's optional mean divides each decoded binary32
+//     value by the rank count (true division), then rounds to bf16.
 
 #include <cmath>
 #include <cstdint>
