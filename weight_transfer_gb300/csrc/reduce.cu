@@ -26,6 +26,23 @@
 namespace fp8q {
 
 constexpr int kRedThreads = 512;
+
+// Four codes of a word -> four binary32.  E5M2 codes go straight from the
+// word's bytes to two f16 pairs (an E5M2 code is the upper byte of the f16 of
+// the same value), without first splitting the word into 16-bit halves:
+// with the split, the k = 8 e5m2 reduce took 32.8 us against 30.7 us.
+template <int FMT>
+__device__ __forceinline__ void red_decode4(uint32_t w, float* f) {
+    if (FMT == kE5M2) {
+        const uint32_t lo = __byte_perm(w, 0u, 0x1404u), hi = __byte_perm(w, 0u, 0x3424u);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else {
+        decode_fp8x4<FMT>(w, f);
+    }
+}
+
 constexpr int kRedTile = 4096;
 constexpr int kRedStages = 3;
 
@@ -147,7 +164,7 @@ dequant_reduce_kernel(ShardPtrs sh, int k, size_t n, uint16_t* __restrict__ out_
                 for (int r = 0; r < KMAX; ++r) {
                     if (r < k) {
                         float d[4];
-                        decode_fp8x4<FMT>(w[r], d);
+                        red_decode4<FMT>(w[r], d);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float p = __fmul_rn(d[q], sc[r]);
