@@ -553,37 +553,99 @@ def _oracle_inputs():
     return _ORACLE_INPUTS
 
 
-def _oracle_step(orc, shards, mats):
+def _oracle_step(orc, shards, mats, keep=None):
     """One step of the oracle on the given slices of the bucket shards and
-    the layer tensors: returns (algorithmic bytes, elements)."""
+    the layer tensors: returns (algorithmic bytes, elements).  With `keep` (a
+    dict), its results are stored there for the parity check of the GPU step."""
     k = len(shards)
     n = shards[0].size
     nbytes = elems = 0
     if n:
         q = {}
+        red = {}
+        hops = []
         for f in (0, 1):
             q[f] = [orc.quantize_blockwise(sh, f) for sh in shards]
             nbytes += bytes_quantize(k * n)
             elems += k * n
         for f in (0, 1):
-            orc.dequant_reduce([c for c, _ in q[f]], [s for _, s in q[f]], f)
+            red[f] = orc.dequant_reduce([c for c, _ in q[f]], [s for _, s in q[f]], f)
             nbytes += bytes_reduce(n, k)
             elems += n
         c, s = q[0][0]
         for h in range(1, k):
-            c, s, _ = orc.ring_hop(c, s, shards[h], 0)
+            c, s, hb = orc.ring_hop(c, s, shards[h], 0)
+            hops.append((c, s, hb))
             nbytes += bytes_hop(n, h == k - 1)
             elems += n
-    for x, b, m, kk in mats:
+        if keep is not None:
+            keep.update(n=n, q=q, red=red, hops=hops)
+    for t, (x, b, m, kk) in enumerate(mats):
         if b * m == 0:
             continue
-        orc.mxfp8_quantize_swizzled(x, b, m, kk)
+        mc, ms = orc.mxfp8_quantize_swizzled(x, b, m, kk)
+        if keep is not None:
+            keep.setdefault("mx", []).append((t, b, m, kk, mc, ms))
         nbytes += bytes_mxfp8(b, m, kk, orc.swizzled_scale_bytes(b, m, kk))
         elems += b * m * kk
     return nbytes, elems
 
 
-def oracle_sample(fraction, threads=1):
+def parity_against_oracle(ds, keep):
+    """The GPU step's own outputs (device set `ds`, rank 0's data) against the
+    oracle's results on the cpu_baseline sample, the same leading elements of
+    every output: codes and scales of both quantizes, both reduce outputs, all
+    7 hops (codes, scales, the last hop's bf16) and the MXFP8 codes and
+    swizzled scales of the sampled experts / rows.  Bit for bit."""
+    import numpy as np
+    import torch
+
+    def host(t, count):
+        v = t.contiguous().view(-1)[:count]
+        if v.dtype in (torch.bfloat16, torch.float16):
+            v = v.view(torch.int16)
+        return v.cpu().numpy().view(np.uint8)
+
+    def raw(a):
+        return np.ascontiguousarray(a).view(np.uint8).ravel()
+
+    checked = mismatched = 0
+
+    def cmp(gpu_bytes, want):
+        nonlocal checked, mismatched
+        want = raw(want)
+        assert gpu_bytes.size == want.size, (gpu_bytes.size, want.size)
+        checked += want.size
+        mismatched += int(np.count_nonzero(gpu_bytes != want))
+    elements = 0
+    if "n" in keep:
+        n = keep["n"]
+        nb = nscales(n)
+        for f in (0, 1):
+            c, sc = ds.q[f]
+            for r, (ec, es) in enumerate(keep["q"][f]):
+                cmp(host(c[r], n), ec)
+                cmp(host(sc[r], nb), es)
+            eb, ef = keep["red"][f]
+            cmp(host(ds.red[f][0], n), eb)
+            cmp(host(ds.red[f][1], n), ef)
+            elements += (len(keep["q"][f]) + 1) * n
+        for h, (ec, es, eb) in enumerate(keep["hops"]):
+            oc, osc = ds.hops[h]
+            cmp(host(oc, n), ec)
+            cmp(host(osc, nb), es)
+            elements += n
+        cmp(host(ds.ring_bf16, n), keep["hops"][-1][2])
+    for t, b, m, kk, mc, ms in keep.get("mx", []):
+        c, sc, _ = ds.mx[t]
+        cmp(host(c, b * m * kk), mc)
+        cmp(host(sc, ms.size), ms)
+        elements += b * m * kk
+    return {"elements": elements, "bytes_compared": checked, "mismatches": mismatched,
+            "what": "the GPU step's outputs against the oracle's on the cpu_baseline sample, byte for byte"}
+
+
+def oracle_sample(fraction, threads=1, keep=None):
     """The oracle on a contiguous fraction of the same workload (rank 0's
     data): returns (algorithmic bytes, elements, seconds, description).  With
     threads > 1 the sample is cut into that many disjoint, 128-aligned parts
@@ -617,7 +679,7 @@ def oracle_sample(fraction, threads=1):
     parts = [part(i, threads) for i in range(threads)]
     t0 = time.perf_counter()
     if threads == 1:
-        res = [_oracle_step(orc, *parts[0])]
+        res = [_oracle_step(orc, *parts[0], keep=keep)]
     else:
         with cf.ThreadPoolExecutor(threads) as ex:
             res = list(ex.map(lambda p_: _oracle_step(orc, *p_), parts))
@@ -1315,6 +1377,11 @@ def main():
 
     fvn = fused_vs_naive(wl, torch)
     sweep = ring_sweep(wl, torch)
+    # a bounded copy wait that ran out leaves invalid outputs and an error
+    # bit: every rank reads its bits before reporting anything
+    dev_errors = wl.w.fp8q_device_errors(clear=False)
+    if dev_errors:
+        raise RuntimeError(f"rank {rank}: a kernel raised device error bits {dev_errors:#x}")
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -1380,9 +1447,12 @@ def main():
                            for k, v in sweep.items()},
         "clocks": clock_info,
         "cpu_baseline": None,
+        "parity_checked": None,
     }
     if world == 1 and not args.no_cpu_baseline:
-        nbytes, elems, dt, desc = oracle_sample(oracle_fraction_for(10.0))
+        keep = {}
+        nbytes, elems, dt, desc = oracle_sample(oracle_fraction_for(10.0), keep=keep)
+        line["parity_checked"] = parity_against_oracle(wl.sets[0], keep)
         line["cpu_baseline"] = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": desc, "seconds": round(dt, 2), "host": host_cpu()}
         ncores = len(os.sched_getaffinity(0))
@@ -1394,7 +1464,12 @@ def main():
             line["cpu_baseline_all_cores"] = {"value": round(nb_all / dt_all / 1e9, 4), "unit": "GB/s",
                                               "cores": ncores, "kind": "oracle", "sample": desc_all,
                                               "seconds": round(dt_all, 2)}
+    line["device_errors"] = wl.w.fp8q_device_errors(clear=False)
     print(json.dumps(line), flush=True)
+    if line["device_errors"]:
+        raise RuntimeError(f"a kernel raised device error bits {line['device_errors']:#x}")
+    if line["parity_checked"] and line["parity_checked"]["mismatches"]:
+        raise RuntimeError(f"the GPU step differs from the oracle: {line['parity_checked']}")
     if world > 1:
         dist.destroy_process_group()
 

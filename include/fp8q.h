@@ -386,6 +386,26 @@ int fp8q_set_launch_overlap(int enable);
 #define FP8Q_DEVICE_ERR_COPY_TIMEOUT 1u
 fp8q_status_t fp8q_device_errors(unsigned int* flags, int clear);
 
+/* Self-test of the bounded copy wait (a test hook, not a step of the codec).
+ * Every staged kernel waits for its shared-memory copies with a wall-clock
+ * limit of 2 s; when a wait runs out, the kernel raises
+ * FP8Q_DEVICE_ERR_COPY_TIMEOUT and returns instead of hanging ([P3] Safety:
+ * fail loudly).  This entry point launches one CTA of 64 threads that waits
+ * on a shared-memory barrier armed for 16 transaction bytes, with the same
+ * wait and the same give-up path, at a limit of `limit_ns`:
+ *   - src == dst == NULL: no copy is issued, so the wait must run out after
+ *     limit_ns; the CTA raises FP8Q_DEVICE_ERR_COPY_TIMEOUT (read back with
+ *     fp8q_device_errors) and returns.  Nothing is in flight at any time, and
+ *     the context stays usable for the calls that follow.
+ *   - src, dst non-NULL (16-byte aligned device pointers, not overlapping):
+ *     the 16 bytes at src are bulk-copied into the barrier's stage, the wait
+ *     completes, and thread 0 writes them to dst; no error bit is raised.
+ * limit_ns must lie in [FP8Q_SELFTEST_MIN_WAIT_NS, FP8Q_SELFTEST_MAX_WAIT_NS]
+ * (FP8Q_ERR_SIZE otherwise); only one of src and dst NULL is FP8Q_ERR_NULL. */
+#define FP8Q_SELFTEST_MIN_WAIT_NS 1000000ull      /* 1 ms */
+#define FP8Q_SELFTEST_MAX_WAIT_NS 2000000000ull   /* 2 s, the kernels' own limit */
+fp8q_status_t fp8q_selftest_copy_wait(const void* src, void* dst, uint64_t limit_ns, fp8q_stream_t stream);
+
 /* Plain satfinite round-to-nearest-even conversion of n binary32 values to
  * FP8 codes, with no scale (the element conversion step of (a) and (c),
  * exposed for exhaustive checking and for per-tensor scaled callers).
@@ -424,8 +444,10 @@ fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const flo
  * and outputs, but no workspace.
  *
  * The scratch is one static device array of FP8Q_STATIC_SCRATCH_FLOATS
- * floats (16 MiB) in the library, reserved on every GPU that loads the
- * library until the process exits.  Each shard uses fp8q_unfused_stride(n)
+ * floats (16 MiB) in the library.  It is reserved on a device when the
+ * library's reduce module is loaded there -- under CUDA's default lazy
+ * module loading, at the first use on that device of this call or of any
+ * other reduce kernel of the library -- and held until the process exits.  Each shard uses fp8q_unfused_stride(n)
  * floats of it, so the call needs k * fp8q_unfused_stride(n) <=
  * FP8Q_STATIC_SCRATCH_FLOATS; larger calls return FP8Q_ERR_SIZE and launch
  * nothing.  The call allocates nothing: no cudaMalloc, no cudaFree.

@@ -19,12 +19,24 @@
  * this path (the conditions are stated next to the kernel).
  *
  * A second mode samples binary32 dividends (24-bit significands, where
- * exhaustion is out of reach) for the two-step form the ring hop uses:
- * Markstein's theorem already proves it exact; the sample is a cross-check.
+ * exhaustion over every divisor is out of reach) for the two-step form the
+ * ring hop uses for its elements: Markstein's theorem already proves it
+ * exact; the sample is a cross-check.
+ *
+ * A third mode covers the block scale RN(amax / Fmax).  There the divisor is
+ * one of two constants, Fmax = 448 (e4m3) or 57344 (e5m2), with the constant
+ * reciprocal y = RN(1 / Fmax), and the dividend amax is a bf16 value in the
+ * quantizer but the binary32 amax of the fp32 sum y in the ring hop.  With
+ * the divisor fixed, every binary32 dividend of a binade is enumerable: the
+ * mode checks the one-step sequence against the IEEE quotient for all 2^23
+ * significands in each of several binades (from 2^-78, the smallest amax the
+ * kernel sends down this path, up to 2^127) and for both constants.
  *
  * Build: cc -O2 -ffp-contract=off -pthread check.c -lm
  *   check bf16 [threads]      exhaustive one-step check (2^30 pairs)
  *   check f32 [count] [seed]  random two-step check
+ *   check scale               exhaustive one-step check of RN(a / Fmax) for
+ *                             binary32 a, Fmax in {448, 57344}
  * Prints the number of mismatching pairs and exits 0 only if it is 0.
  */
 #include <math.h>
@@ -81,7 +93,34 @@ static int random_f32(uint64_t count, uint64_t seed) {
     return bad != 0;
 }
 
+/* One step from the constant reciprocal, every binary32 significand of the
+ * binades 2^e, e in the list, for both format maxima. */
+static int scale_constants(void) {
+    static const float dmax[2] = {448.0f, 57344.0f};
+    static const int binades[] = {-78, -77, -40, -1, 0, 1, 17, 60, 126, 127};
+    const int nbin = (int)(sizeof binades / sizeof binades[0]);
+    uint64_t bad = 0, checked = 0;
+    for (int f = 0; f < 2; ++f) {
+        const float d = dmax[f];
+        const float y = 1.0f / d;
+        for (int b = 0; b < nbin; ++b) {
+            const uint32_t ebits = (uint32_t)(binades[b] + 127) << 23;
+            for (uint32_t m = 0; m < (1u << 23); ++m) {
+                const float a = f_of(ebits | m);
+                const float q0 = a * y;
+                const float r = fmaf(q0, d, -a);
+                const float q1 = fmaf(-r, y, q0);
+                bad += u_of(q1) != u_of(a / d);
+            }
+            checked += 1u << 23;
+        }
+    }
+    printf("checked %llu dividends, mismatches %llu\n", (unsigned long long)checked, (unsigned long long)bad);
+    return bad != 0;
+}
+
 int main(int argc, char** argv) {
+    if (argc > 1 && strcmp(argv[1], "scale") == 0) return scale_constants();
     if (argc > 1 && strcmp(argv[1], "f32") == 0)
         return random_f32(argc > 2 ? strtoull(argv[2], 0, 0) : 100000000ull, argc > 3 ? strtoull(argv[3], 0, 0) : 1);
     int nt = argc > 2 ? atoi(argv[2]) : 8;

@@ -259,3 +259,13 @@ def test_ring_group_and_allreduce_validation(L):
     # results of two ranks in one place
     same = (ctypes.c_void_p * 2)(A + 20 * MB, A + 20 * MB)
     assert rx(pp, same, 2, 1024, 0, A + 40 * MB, 1 << 20, None, w.FP8Q_ALLREDUCE_MEAN, None) == ERR_ALIAS
+
+
+def test_selftest_copy_wait_validation(L):
+    t = L.fp8q_selftest_copy_wait
+    assert t(None, None, 999_999, None) == ERR_SIZE                 # below 1 ms
+    assert t(None, None, 2_000_000_001, None) == ERR_SIZE           # above the kernels' own 2 s
+    assert t(A, None, 10_000_000, None) == ERR_NULL                  # src without dst
+    assert t(None, A, 10_000_000, None) == ERR_NULL
+    assert t(A + 8, A + MB, 10_000_000, None) == ERR_ALIGN
+    assert t(A, A, 10_000_000, None) == ERR_ALIAS

@@ -476,6 +476,49 @@ def test_swizzle_is_a_bijection_onto_the_unpadded_cells(orc, m, kb):
         assert len(seen) == total                     # no padding: onto
 
 
+def tiled_128x4(nat, m, kb):
+    """The block-scaled GEMM scale layout written as array reshapes (NVIDIA
+    cuBLAS documentation, "1D Block Scaling Factors Layout"): a [rows, K/32]
+    scale matrix is zero-padded to whole 128 x 4 tiles; tile (row tile a,
+    column tile b) holds 32 lines of 16 bytes, line i carrying, for rows
+    i, i + 32, i + 64 and i + 96 of the row tile, their 4 scales; tiles are
+    stored row tile by row tile.  nat: [batch, m, kb] -> flat [batch, ...]."""
+    bt = nat.shape[0]
+    mp, kp = -(-m // 128) * 128, -(-kb // 4) * 4
+    pad = np.zeros((bt, mp, kp), nat.dtype)
+    pad[:, :m, :kb] = nat
+    # row = a*128 + g*32 + i, column = b*4 + c  ->  order (a, b, i, g, c)
+    t = pad.reshape(bt, mp // 128, 4, 32, kp // 4, 4).transpose(0, 1, 4, 3, 2, 5)
+    return t.reshape(-1)
+
+
+@pytest.mark.parametrize("bt,m,kb", [(1, 1, 1), (2, 129, 3), (1, 256, 8), (2, 384, 24), (1, 200, 64)])
+def test_swizzle_equals_the_reshape_form_of_128x4_tiles(orc, bt, m, kb):
+    ids = np.arange(1, bt * m * kb + 1, dtype=np.int64).reshape(bt, m, kb)
+    want = tiled_128x4(ids, m, kb)
+    got = np.zeros(orc.swizzled_scale_bytes(bt, m, kb * 32), np.int64)
+    for b in range(bt):
+        for r in range(m):
+            for j in range(kb):
+                got[orc.swizzle_offset(b, r, j, m, kb)] = ids[b, r, j]
+    assert np.array_equal(got, want)
+
+
+def test_swizzled_scales_are_the_reshape_form_of_the_row_major_exponents(orc):
+    # the whole scale buffer of a ragged batch: the E8M0 byte of each
+    # 32-block, from the block amax alone, laid out by the reshape form
+    rng = np.random.default_rng(11)
+    bt, m, k = 2, 200, 96
+    x = (rng.standard_normal((bt, m, k)) * np.exp2(rng.integers(-20, 20, (bt, m, 1)))).astype(np.float32)
+    x[0, 3, 32:64] = 0.0                                      # a zero block
+    w = bf16_bits(x.ravel())
+    amax = np.abs(bf16_val(w).reshape(bt, m, k // 32, 32)).max(axis=3)
+    nat = np.vectorize(orc.e8m0_of_amax)(amax).astype(np.int64)
+    assert nat[0, 3, 1] == 0
+    _, sc = orc.mxfp8_quantize_swizzled(w, bt, m, k)
+    assert np.array_equal(sc.astype(np.int64), tiled_128x4(nat, m, k // 32))
+
+
 def test_mxfp8_k32_keeps_its_scale_column_and_zero_padding(orc):
     # K == 32: one real scale column, padded to a 4-wide tile with zeros
     rng = np.random.default_rng(4)

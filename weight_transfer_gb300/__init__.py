@@ -66,6 +66,7 @@ FP8Q_MAX_QUANT_GROUP = 16
 FP8Q_HOP_LOCAL_READY = 1
 FP8Q_INPUTS_READY = 1
 FP8Q_ALLREDUCE_MEAN = 1
+FP8Q_DEVICE_ERR_COPY_TIMEOUT = 1
 
 
 class mxfp8_tensor_t(ctypes.Structure):
@@ -124,6 +125,7 @@ _SIGNATURES = {
     "fp8q_last_cuda_error": ([], _int),
     "fp8q_set_launch_overlap": ([_int], _int),
     "fp8q_device_errors": ([ctypes.POINTER(ctypes.c_uint), _int], _int),
+    "fp8q_selftest_copy_wait": ([_vp, _vp, ctypes.c_uint64, _vp], _int),
     "fp8q_encode_f32": ([_vp, _sz, _int, _vp, _vp], _int),
     "fp8q_dequantize": ([_vp, _vp, _sz, _int, _vp, _vp, _vp], _int),
     "fp8q_unfused_stride": ([_sz], _sz),
@@ -194,6 +196,17 @@ def fp8q_device_errors(clear: bool = True) -> int:
     v = ctypes.c_uint(0)
     _check("fp8q_device_errors", lib().fp8q_device_errors(ctypes.byref(v), int(clear)))
     return int(v.value)
+
+
+def fp8q_selftest_copy_wait(limit_ns: int, src: Optional[torch.Tensor] = None, dst: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """Test hook of the kernels' bounded copy wait: with no src/dst the wait
+    runs out after limit_ns and raises FP8Q_DEVICE_ERR_COPY_TIMEOUT (read it
+    with fp8q_device_errors); with 16-byte src/dst buffers the copy lands and
+    src's 16 bytes are written to dst."""
+    st = lib().fp8q_selftest_copy_wait(_dev(src, "src", numel=None), _dev(dst, "dst", numel=None), int(limit_ns),
+                                       _stream(stream))
+    _check("fp8q_selftest_copy_wait", st)
 
 
 def fp8q_set_launch_overlap(enable: bool) -> bool:

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8q.so")
 
-SOURCES = ["api.cu", "quantize.cu", "reduce.cu", "ring_hop.cu", "mxfp8.cu", "mxfp8_receive.cu", "ring_allreduce.cu", "tensorwise.cu", "pack.cu"]
+SOURCES = ["api.cu", "quantize.cu", "reduce.cu", "ring_hop.cu", "mxfp8.cu", "mxfp8_receive.cu", "ring_allreduce.cu", "tensorwise.cu", "pack.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
                   "-fmad=false", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC]

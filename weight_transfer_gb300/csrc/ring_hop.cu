@@ -183,6 +183,8 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        // a is a binary32 amax here, not a bf16 one: block_scale is exact for
+        // every binary32 dividend (its constant divisor makes that checkable)
         const float sc = block_scale<FMT>(a);
         float q[16];
         block_quotients<2, 16>(y, sc, q);
