@@ -111,8 +111,10 @@ def test_gemm_reads_each_weight_scale_where_the_layout_puts_it(w, orc, m, n, k):
     check_product(w, orc, blocky(m, k, seed=m + k), selector(n, k, seed=n + k + 1))
 
 
-@pytest.mark.parametrize("m,n,k", [(128, 256, 32), (128, 4096, 2048), (128, 200, 96)])
+@pytest.mark.parametrize("m,n,k", [(128, 256, 32), (128, 4096, 2048), (128, 208, 96)])
 def test_gemm_reads_each_second_operand_scale_where_the_layout_puts_it(w, orc, m, n, k):
+    # the GEMM wants the second operand's row count divisible by 16 (208 still
+    # pads its last 128-row scale tile)
     check_product(w, orc, selector(m, k, seed=m + k + 2), blocky(n, k, seed=n + k + 3))
 
 
