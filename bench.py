@@ -983,8 +983,10 @@ def extra_rows(wl, torch, peak):
     out["ring_allreduce_sim_256MiB_per_rank"] = {
         "ranks": P, "elements": nl_, "ms": round(ms, 4), "kernel_bytes": kb2,
         "GB/s": round(kb2 / (ms * 1e-3) / 1e9, 1), "frac_of_peak": round(kb2 / (ms * 1e-3) / 1e9 / peak, 4)}
+    del bws
+    out["ring_allreduce_sim_256MiB_per_rank"]["breakdown"] = allreduce_breakdown(w, torch, dev, st, big, bres, peak)
     out["ring_allreduce_sim"]["frac_of_peak"] = round(out["ring_allreduce_sim"]["GB/s"] / peak, 4)
-    del big, bres, bws
+    del big, bres
     name, b, mm, kk = wl.tensors[0]
     c, sc, sb = ds.mx[0]
     outw = torch.empty((b, mm, kk), dtype=torch.bfloat16, device=dev)
@@ -1029,6 +1031,85 @@ def extra_rows(wl, torch, peak):
                                   "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
                                   "frac_of_peak": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
     return out
+
+
+def allreduce_breakdown(w, torch, dev, st, parts, res_one_call, peak, reps=10):
+    """The simulated ring AllReduce's launches one by one: the same schedule
+    as fp8q_ring_allreduce_sim, replayed through the public entry points
+    (one grouped quantize, P - 1 hop groups, the all-gather decode), with
+    events around each launch (median of `reps`, L2 flushed before each
+    pass) and around the whole sequence.  Its results must equal the
+    one-call collective's, byte for byte."""
+    L = w.lib()
+    vp = ctypes.c_void_p
+    P, n = len(parts), parts[0].numel()
+    m = n // P
+    u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+    msg = [[(torch.empty(m, dtype=u8, device=dev), torch.empty(nscales(m), dtype=f32, device=dev)) for _ in range(P)]
+           for _ in range(2)]
+    fin_c = torch.empty(n, dtype=u8, device=dev)
+    fin_s = torch.empty(nscales(n), dtype=f32, device=dev)
+    res = [torch.empty(n, dtype=bf, device=dev) for _ in range(P)]
+    sp = vp(st.cuda_stream)
+    steps = []
+    items = (w.fp8q_quant_t * P)(*[w.fp8q_quant_t(parts[i].data_ptr() + 2 * i * m, m, msg[0][i][0].data_ptr(),
+                                                  msg[0][i][1].data_ptr()) for i in range(P)])
+    steps.append(("quantize_group", P * bytes_quantize(m),
+                  lambda: L.fp8q_quantize_blockwise_group(items, P, 0, ctypes.c_uint(0), sp)))
+    keep = [items]
+    for s_ in range(1, P):
+        hops = (w.fp8q_hop_t * P)()
+        for i in range(P):
+            frm, c = (i - 1) % P, (i - s_) % P
+            ic, isc = msg[(s_ - 1) & 1][frm]
+            if s_ < P - 1:
+                oc, osc = msg[s_ & 1][i][0].data_ptr(), msg[s_ & 1][i][1].data_ptr()
+            else:
+                oc, osc = fin_c.data_ptr() + c * m, fin_s.data_ptr() + 4 * c * (m // 128)
+            hops[i] = w.fp8q_hop_t(ic.data_ptr(), isc.data_ptr(), parts[i].data_ptr() + 2 * c * m, m, oc, osc, None)
+        keep.append(hops)
+        steps.append((f"hop_group_{s_}", P * bytes_hop(m, False),
+                      (lambda h=hops: L.fp8q_ring_hop_group_ex(h, P, 0, ctypes.c_uint(w.FP8Q_HOP_LOCAL_READY), sp))))
+    outs = (vp * P)(*[r.data_ptr() for r in res])
+    steps.append(("gather_decode", n + 4 * nscales(n) + P * 2 * n,
+                  lambda: L.fp8q_gather_decode(vp(fin_c.data_ptr()), vp(fin_s.data_ptr()), n, 0, outs, P,
+                                               ctypes.c_uint(0), sp)))
+    flush = L2Flush(torch, dev)
+    Ev = torch.cuda.Event
+    per = [[] for _ in steps]
+    whole = []
+    for rep in range(reps + 1):
+        flush()
+        evs = [(Ev(enable_timing=True), Ev(enable_timing=True)) for _ in steps]
+        for (name, _, fn), (a, b) in zip(steps, evs):
+            a.record(st)
+            if fn() != 0:
+                raise RuntimeError(f"AllReduce breakdown: {name} failed")
+            b.record(st)
+        flush()
+        a0, b0 = Ev(enable_timing=True), Ev(enable_timing=True)
+        a0.record(st)
+        for _, _, fn in steps:
+            fn()
+        b0.record(st)
+        torch.cuda.synchronize(dev)
+        if rep:
+            for i, (a, b) in enumerate(evs):
+                per[i].append(a.elapsed_time(b))
+            whole.append(a0.elapsed_time(b0))
+    equal = all(torch.equal(a, b) for a, b in zip(res, res_one_call))
+    rows = []
+    for (name, nbytes, _), t in zip(steps, per):
+        us = 1e3 * sorted(t)[len(t) // 2]
+        rows.append({"launch": name, "us": round(us, 2), "bytes": nbytes,
+                     "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac_of_peak": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)})
+    wm = sorted(whole)[len(whole) // 2]
+    return {"launches": rows, "sequence_ms": round(wm, 4),
+            "sum_of_launches_ms": round(sum(r["us"] for r in rows) / 1e3, 4),
+            "results_equal_one_call": equal,
+            "timing": "events around each launch (no overlap between launches), and around the whole sequence "
+                      "(dependent launch as in the one-call collective)"}
 
 
 def vec3p5b_row(wl, torch, peak, reps=3):
@@ -1116,6 +1197,73 @@ def vec3p5b_row(wl, torch, peak, reps=3):
                                 "GB/s": round(rb / (r_med * 1e-3) / 1e9, 1),
                                 "frac_of_peak": round(rb / (r_med * 1e-3) / 1e9 / peak, 4)},
             "inputs": "device Philox normal, seeds 100 + shard, with the vector's outliers and zero blocks"}
+
+
+def mxfp8_stack_row(wl, torch, peak, layers=48, reps=3):
+    """MXFP8 prequantization of a whole Qwen3-30B-A3B-shaped stack: 48 layers
+    (29.9e9 weights, 59.8 GB of bf16) resident on the device, one grouped
+    launch per layer, launched back to back (times: medians of `reps` passes
+    over the stack).  A second pass puts events between the layers and gives
+    the spread of the per-layer rate.  The weights are drawn on the device
+    from seeded Philox normals with the stack's distribution (N(0, 0.02^2),
+    1% of rows x50): the counter-based host generator would need minutes for
+    29.9e9 values."""
+    import gen
+    w, dev, st = wl.w, wl.dev, wl.stream
+    L = w.lib()
+    tensors = gen.QWEN3_TENSORS
+    per_layer = sum(3 * b * m * k + w.mxfp8_swizzled_scale_bytes(b, m, k) for _, b, m, k in tensors)
+    free, _ = torch.cuda.mem_get_info(dev)
+    if free < layers * per_layer * 1.05 + (2 << 30):
+        return {"skipped": f"needs {layers * per_layer / 2**30:.1f} GiB, {free / 2**30:.1f} GiB free"}
+    g = torch.Generator(device=dev)
+    keep, groups = [], []
+    for l in range(layers):
+        arr = (w.mxfp8_tensor_t * len(tensors))()
+        for t, (name, b, m, k) in enumerate(tensors):
+            g.manual_seed(10_000 + 100 * l + t)
+            x32 = torch.randn((b, m, k), device=dev, generator=g).mul_(0.02)
+            rows = torch.rand((b, m, 1), device=dev, generator=g) < 0.01
+            x = torch.where(rows, x32 * 50.0, x32).to(torch.bfloat16)
+            del x32, rows
+            c = torch.empty((b, m, k), dtype=torch.uint8, device=dev)
+            sc = torch.empty(w.mxfp8_swizzled_scale_bytes(b, m, k), dtype=torch.uint8, device=dev)
+            arr[t] = w.mxfp8_tensor_t(x.data_ptr(), b, m, k, c.data_ptr(), sc.data_ptr())
+            keep += [x, c, sc]
+        groups.append(arr)
+    torch.cuda.synchronize(dev)
+    sp = ctypes.c_void_p(st.cuda_stream)
+    ready = ctypes.c_uint(w.FP8Q_INPUTS_READY)
+    Ev = torch.cuda.Event
+    whole, per = [], []
+    for rep in range(reps + 1):
+        a, b_ = Ev(enable_timing=True), Ev(enable_timing=True)
+        a.record(st)
+        for arr in groups:
+            if L.mxfp8_quantize_swizzled_group_ex(arr, len(tensors), ready, sp) != 0:
+                raise RuntimeError("MXFP8 stack launch failed")
+        b_.record(st)
+        torch.cuda.synchronize(dev)
+        if rep:
+            whole.append(a.elapsed_time(b_))
+    evs = [(Ev(enable_timing=True), Ev(enable_timing=True)) for _ in groups]
+    for arr, (a, b_) in zip(groups, evs):
+        a.record(st)
+        L.mxfp8_quantize_swizzled_group_ex(arr, len(tensors), ready, sp)
+        b_.record(st)
+    torch.cuda.synchronize(dev)
+    per = sorted(per_layer / (a.elapsed_time(b_) * 1e-3) / 1e9 for a, b_ in evs)
+    ms = sorted(whole)[len(whole) // 2]
+    total = layers * per_layer
+    del keep, groups
+    torch.cuda.empty_cache()
+    return {"layers": layers, "weights": layers * sum(b * m * k for _, b, m, k in tensors), "bytes": total,
+            "ms": round(ms, 3), "GB/s": round(total / (ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(total / (ms * 1e-3) / 1e9 / peak, 4),
+            "per_layer_GBps": {"min": round(per[0], 1), "median": round(per[len(per) // 2], 1),
+                               "max": round(per[-1], 1)},
+            "launches": f"{layers} grouped launches (7 tensors each) back to back; medians of {reps} passes",
+            "inputs": "device Philox normal N(0, 0.02^2), 1% of rows x50, seed 10000 + 100 * layer + tensor"}
 
 
 def graph_timed(wl, torch, flush, steps, dom, barrier, clocks):
@@ -1228,6 +1376,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-vec3p5b", action="store_true", help="skip the 3.5e9-element vector row")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 48-layer MXFP8 stack row")
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES) + ["mxfp8_dequantize", "ring_allreduce_sim"],
                     help="launch one kernel of the step a few times on its bench inputs and exit (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=3)
@@ -1392,6 +1541,8 @@ def main():
     extras = extra_rows(wl, torch, peak)
     if not args.no_vec3p5b:
         extras["vec3p5b"] = vec3p5b_row(wl, torch, peak)
+    if not args.no_stack:
+        extras["mxfp8_48_layers"] = mxfp8_stack_row(wl, torch, peak)
     total_ms = sum(d["ms"] for d in per_kind.values())
     kernels = {}
     for kind, d in per_kind.items():

@@ -229,6 +229,19 @@ fp8q_status_t fp8q_ring_allreduce_sim_ex(const void* const* partials, void* cons
                                          fp8q_format_t fmt, void* workspace, size_t workspace_bytes,
                                          uint64_t* wire_bytes, unsigned int flags, fp8q_stream_t stream);
 
+/* The all-gather receiver step of the ring AllReduce above, on its own:
+ * one FP8 vector (n codes and their fp8q_num_scales(n) block scales, the
+ * fully reduced chunks in chunk order) decoded once and written as bf16 to
+ * each of `count` outputs, outs[o][i] = RNE_bf16(RN(decode(c_i) * s_b)).
+ * With FP8Q_ALLREDUCE_MEAN each decoded value is first divided by `count`
+ * (a true binary32 division), as fp8q_ring_allreduce_sim_ex does.
+ *   outs  : HOST array of `count` device pointers to n bf16 each
+ *   count : 1 .. FP8Q_MAX_HOP_GROUP (FP8Q_ERR_K otherwise)
+ * Outputs may not overlap each other or the inputs (FP8Q_ERR_ALIAS); other
+ * flag bits: FP8Q_ERR_FLAGS. */
+fp8q_status_t fp8q_gather_decode(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                                 void* const* outs, int count, unsigned int flags, fp8q_stream_t stream);
+
 /* ------------------------------------------------------------ variants ----
  * fp8q_quantize_tensorwise: one scale for the whole tensor (the tensorwise
  *   recipe of TorchAO's Float8Linear that [P2] uses for its FP8 GEMMs):

@@ -269,3 +269,19 @@ def test_selftest_copy_wait_validation(L):
     assert t(None, A, 10_000_000, None) == ERR_NULL
     assert t(A + 8, A + MB, 10_000_000, None) == ERR_ALIGN
     assert t(A, A, 10_000_000, None) == ERR_ALIAS
+
+
+def test_gather_decode_validation(L):
+    gd = L.fp8q_gather_decode
+    outs = (ctypes.c_void_p * 2)(A + 8 * MB, A + 16 * MB)
+    assert gd(A, A + MB, 4096, 0, outs, 2, 2, None) == ERR_FLAGS
+    assert gd(A, A + MB, 4096, 0, outs, 0, 0, None) == ERR_K
+    assert gd(A, A + MB, 4096, 0, outs, 17, 0, None) == ERR_K
+    assert gd(A, A + MB, 4096, 7, outs, 2, 0, None) == ERR_FORMAT
+    assert gd(None, A + MB, 4096, 0, outs, 2, 0, None) == ERR_NULL
+    assert gd(A + 4, A + MB, 4096, 0, outs, 2, 0, None) == ERR_ALIGN
+    same = (ctypes.c_void_p * 2)(A + 8 * MB, A + 8 * MB + 4096)
+    assert gd(A, A + MB, 4096, 0, same, 2, 0, None) == ERR_ALIAS
+    over_in = (ctypes.c_void_p * 1)(A)
+    assert gd(A, A + MB, 4096, 0, over_in, 1, 0, None) == ERR_ALIAS
+    assert gd(None, None, 0, 0, outs, 2, 0, None) == OK                 # empty: no-op

@@ -131,6 +131,25 @@ def test_mxfp8_group_whole_qwen3_layer(w, orc):
     pool.shutdown()
 
 
+@pytest.mark.parametrize("layer", [0, 23, 47])
+def test_mxfp8_stack_layers_sampled(w, orc, layer):
+    # the first, a middle and the last layer of the 48-layer stack, each in
+    # the bench's one grouped launch; the oracle checks every attention
+    # matrix in full and experts 0, 64 and 127 of each expert tensor
+    xs = [gen.qwen3_tensor(layer, t) for t in range(len(gen.QWEN3_TENSORS))]
+    codes, scales = w.mxfp8_quantize_swizzled_group([x.cuda() for x in xs])
+    torch.cuda.synchronize()
+    for t, (name, b, m, k) in enumerate(gen.QWEN3_TENSORS):
+        hb = bits16(xs[t]).reshape(b, m * k)
+        per = w.mxfp8_swizzled_scale_bytes(1, m, k)
+        gc = u8(codes[t]).reshape(b, m * k)
+        gs = u8(scales[t]).reshape(b, per)
+        for e in ([0] if b == 1 else [0, 64, 127]):
+            ec, es = orc.mxfp8_quantize_swizzled(hb[e].copy(), 1, m, k)
+            assert_same(gs[e], es, f"layer {layer} {name}[{e}] scales")
+            assert_same(gc[e], ec, f"layer {layer} {name}[{e}] codes")
+
+
 # ----------------------------------------------------------- receiver side
 @pytest.mark.parametrize("b,m,k", [(1, 1, 32), (3, 129, 96), (2, 256, 768), (1, 300, 2048)])
 def test_mxfp8_dequantize_and_unswizzle(w, orc, b, m, k):

@@ -135,3 +135,19 @@ def test_ring_allreduce_rejects_bad_sizes(w):
     parts = [torch.zeros(1000, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     with pytest.raises(w.Fp8qError):
         w.fp8q_ring_allreduce_sim(parts)          # 1000 is not a multiple of 512 * 2
+
+
+@pytest.mark.parametrize("mean", [False, True])
+@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("count,n", [(1, 4096), (3, 4096 * 5 + 77), (8, 20_000), (16, 4096 * 2 + 4095)])
+def test_gather_decode_matches_oracle(w, orc, fmt, count, n, mean):
+    # every output equals the oracle's dequantize (or its mean over `count`),
+    # including the ragged last tile
+    codes, scales = random_shards(1, n, fmt, seed=500 + count + n)
+    sc = np.minimum(scales[0], np.float32(1e30))
+    outs = w.fp8q_gather_decode(torch.from_numpy(codes[0]).cuda(), torch.from_numpy(sc).cuda(), count, fmt,
+                                mean=mean)
+    torch.cuda.synchronize()
+    want, _ = orc.dequantize_mean(codes[0], sc, fmt, count) if mean else orc.dequantize(codes[0], sc, fmt)
+    for o, t in enumerate(outs):
+        assert_same(bits16(t), want, f"output {o}")

@@ -126,6 +126,7 @@ _SIGNATURES = {
     "fp8q_set_launch_overlap": ([_int], _int),
     "fp8q_device_errors": ([ctypes.POINTER(ctypes.c_uint), _int], _int),
     "fp8q_selftest_copy_wait": ([_vp, _vp, ctypes.c_uint64, _vp], _int),
+    "fp8q_gather_decode": ([_vp, _vp, _sz, _int, ctypes.POINTER(_vp), _int, ctypes.c_uint, _vp], _int),
     "fp8q_encode_f32": ([_vp, _sz, _int, _vp, _vp], _int),
     "fp8q_dequantize": ([_vp, _vp, _sz, _int, _vp, _vp, _vp], _int),
     "fp8q_unfused_stride": ([_sz], _sz),
@@ -410,6 +411,21 @@ def fp8q_ring_allreduce_sim(partials: Sequence[torch.Tensor], fmt="e4m3", result
                                           workspace.numel(), ctypes.byref(wire), flags, _stream(stream))
     _check("fp8q_ring_allreduce_sim_ex", st)
     return list(results), int(wire.value)
+
+
+def fp8q_gather_decode(codes: torch.Tensor, scales: torch.Tensor, count: int, fmt="e4m3",
+                       outs: Optional[Sequence[torch.Tensor]] = None, mean: bool = False, stream=None):
+    """One FP8 vector decoded once into `count` bf16 outputs (the all-gather
+    step of the ring AllReduce); mean=True divides by `count` first."""
+    n = codes.numel()
+    if outs is None:
+        outs = [torch.empty(n, dtype=torch.bfloat16, device=codes.device) for _ in range(count)]
+    op = (_vp * count)(*[_dev(t, f"outs[{i}]", torch.bfloat16, n) for i, t in enumerate(outs)])
+    st = lib().fp8q_gather_decode(_dev(codes, "codes", torch.uint8), _dev(scales, "scales", torch.float32,
+                                                                           fp8q_num_scales(n)),
+                                  n, _fmt(fmt), op, count, FP8Q_ALLREDUCE_MEAN if mean else 0, _stream(stream))
+    _check("fp8q_gather_decode", st)
+    return list(outs)
 
 
 def mxfp8_quantize_swizzled_group(weights: Sequence[torch.Tensor], codes: Optional[Sequence[torch.Tensor]] = None,

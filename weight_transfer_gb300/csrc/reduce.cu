@@ -548,6 +548,13 @@ extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes
 }
 
 // ------------------------------------------------- no-allocation variant ----
+extern "C" fp8q_status_t fp8q_gather_decode(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
+                                            void* const* outs, int count, unsigned int flags, fp8q_stream_t stream) {
+    if (flags & ~FP8Q_ALLREDUCE_MEAN) return FP8Q_ERR_FLAGS;
+    return fp8q::gather_decode_entry(codes, scales, n, fmt, outs, count, (flags & FP8Q_ALLREDUCE_MEAN) ? count : 0,
+                                     stream);
+}
+
 // fp8q_dequant_reduce_unfused with its workspace in a static device array
 // instead of a caller-supplied buffer (for callers that cannot allocate).
 

@@ -23,6 +23,12 @@
 // With FP8Q_HOP_LOCAL_READY the local partials of each CTA's first tiles are
 // copied before the grid-dependency wait, so that they stream in while the
 // previous kernel on the stream drains.
+//
+// A group of two or more hops (every rank's hop of one step of a simulated
+// ring) runs ring_hop_group_kernel: the same tiles and arithmetic, with the
+// per-tile bookkeeping hoisted out of the loop.  The kernel is bound by
+// instruction issue at large sizes (79% issue-active, 20 thread-instructions
+// per element on a 134M-element hop), so per-tile overhead shows directly.
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
@@ -56,8 +62,62 @@ struct HopGroup {
     int local_ready;       // the local partials may be read before the predecessor grid ends
 };
 
-// REQ_BF16: requantize RNE_bf16(y), the bf16 partial a receiver keeps,
-// instead of the fp32 sum y (the alternative reading of the hop).
+// One lane's share of one block: 16 incoming codes (ca, cb) with the block's
+// incoming scale s_in and 16 local bf16 values (la, lb) -> the fp32 sums y,
+// the block's new scale sc (amax over the 8 lanes of the block) and the 16
+// new codes (wa, wb).  REQ_BF16: requantize RNE_bf16(y), the bf16 partial a
+// receiver keeps, instead of the fp32 sum y (the alternative reading of the
+// hop).
+template <int FMT, bool REQ_BF16>
+__device__ __forceinline__ void hop_block16(const uint2& ca, const uint2& cb, const uint4& la, const uint4& lb,
+                                            float s_in, uint32_t (&wa)[2], uint32_t (&wb)[2], float (&y)[16],
+                                            float& sc) {
+    float d[16], lf[16];
+    decode_fp8x4<FMT>(ca.x, d);
+    decode_fp8x4<FMT>(ca.y, d + 4);
+    decode_fp8x4<FMT>(cb.x, d + 8);
+    decode_fp8x4<FMT>(cb.y, d + 12);
+    unpack8(la, *reinterpret_cast<float(*)[8]>(lf));
+    unpack8(lb, *reinterpret_cast<float(*)[8]>(lf + 8));
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        y[i] = __fadd_rn(__fmul_rn(d[i], s_in), lf[i]);
+        if (REQ_BF16) y[i] = bf16_lo(pack_bf16x2(y[i], 0.0f));
+        a = fmaxf(a, fabsf(y[i]));
+    }
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+    // a is a binary32 amax here, not a bf16 one: block_scale is exact for
+    // every binary32 dividend (its constant divisor makes that checkable)
+    sc = block_scale<FMT>(a);
+    float q[16];
+    block_quotients<2, 16>(y, sc, q);
+    wa[0] = cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]);
+    wa[1] = cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7]);
+    wb[0] = cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]);
+    wb[1] = cvt_fp8x4<FMT>(q[12], q[13], q[14], q[15]);
+}
+
+// The lane's 16 sums as bf16 (RNE), at elements e0 .. e0+7 and e0+64 .. e0+71.
+__device__ __forceinline__ void store_hop_bf16(uint16_t* out_bf16, size_t e0, const float (&y)[16], bool staged,
+                                               bool in_range, long long avail) {
+    uint32_t ha[4], hb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ha[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
+        hb[i] = pack_bf16x2(y[8 + 2 * i], y[8 + 2 * i + 1]);
+    }
+    if (staged) {
+        st_stream(out_bf16 + e0, make_uint4(ha[0], ha[1], ha[2], ha[3]));
+        st_stream(out_bf16 + e0 + 64, make_uint4(hb[0], hb[1], hb[2], hb[3]));
+    } else if (in_range) {
+        st_u16_tail(out_bf16 + e0, ha, 4, avail);
+        st_u16_tail(out_bf16 + e0 + 64, hb, 4, avail - 64);
+    }
+}
+
 template <int FMT, bool REQ_BF16>
 __global__ void __launch_bounds__(kHopThreads)
 ring_hop_kernel(const __grid_constant__ HopGroup g) {
@@ -165,31 +225,10 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
             s_in = b < nb ? g.in_scales[h][b] : 0.0f;
         }
 
-        float d[16], lf[16];
-        decode_fp8x4<FMT>(ca.x, d);
-        decode_fp8x4<FMT>(ca.y, d + 4);
-        decode_fp8x4<FMT>(cb.x, d + 8);
-        decode_fp8x4<FMT>(cb.y, d + 12);
-        unpack8(la, *reinterpret_cast<float(*)[8]>(lf));
-        unpack8(lb, *reinterpret_cast<float(*)[8]>(lf + 8));
+        uint32_t wa[2], wb[2];
         float y[16];
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            y[i] = __fadd_rn(__fmul_rn(d[i], s_in), lf[i]);
-            if (REQ_BF16) y[i] = bf16_lo(pack_bf16x2(y[i], 0.0f));
-            a = fmaxf(a, fabsf(y[i]));
-        }
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        // a is a binary32 amax here, not a bf16 one: block_scale is exact for
-        // every binary32 dividend (its constant divisor makes that checkable)
-        const float sc = block_scale<FMT>(a);
-        float q[16];
-        block_quotients<2, 16>(y, sc, q);
-        uint32_t wa[2] = {cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])};
-        uint32_t wb[2] = {cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]), cvt_fp8x4<FMT>(q[12], q[13], q[14], q[15])};
+        float sc;
+        hop_block16<FMT, REQ_BF16>(ca, cb, la, lb, s_in, wa, wb, y, sc);
         uint8_t* out_codes = g.out_codes[h];
         uint16_t* out_bf16 = g.out_bf16[h];
         if (staged) {
@@ -201,21 +240,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
             st_u8_tail(out_codes + e0 + 64, wb, 2, avail - 64);
             if (j == 0) g.out_scales[h][b] = sc;
         }
-        if (out_bf16 != nullptr) {
-            uint32_t ha[4], hb[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                ha[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
-                hb[i] = pack_bf16x2(y[8 + 2 * i], y[8 + 2 * i + 1]);
-            }
-            if (staged) {
-                st_stream(out_bf16 + e0, make_uint4(ha[0], ha[1], ha[2], ha[3]));
-                st_stream(out_bf16 + e0 + 64, make_uint4(hb[0], hb[1], hb[2], hb[3]));
-            } else if (b < nb) {
-                st_u16_tail(out_bf16 + e0, ha, 4, avail);
-                st_u16_tail(out_bf16 + e0 + 64, hb, 4, avail - 64);
-            }
-        }
+        if (out_bf16 != nullptr) store_hop_bf16(out_bf16, e0, y, staged, b < nb, avail);
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
@@ -242,6 +267,163 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
     }
 }
 
+// The same hop for a group of two or more hops (all ranks' hops of one step
+// of a simulated ring), with the per-tile bookkeeping hoisted: the hop index
+// is carried from tile to tile (tiles only move forward), the staged-tile
+// bound of each hop is precomputed on the host, and the stage index is a
+// counter.  With several hops the single-hop kernel's per-tile search over
+// the hop table costs about 14% more instructions, in a kernel that is bound
+// by instruction issue at large sizes (8 hops of 16.8M elements: 108.5 us
+// there, 96.3 us here; the 8-rank AllReduce of 256 MiB per rank 1.11 ->
+// 1.03 ms).  For one hop the carried index made the chain slower, so single
+// hops keep ring_hop_kernel.
+struct HopGroupMulti {
+    const uint8_t* in_codes[kHopMaxGroup];
+    const float* in_scales[kHopMaxGroup];
+    const uint16_t* local[kHopMaxGroup];
+    uint8_t* out_codes[kHopMaxGroup];
+    float* out_scales[kHopMaxGroup];
+    uint16_t* out_bf16[kHopMaxGroup];          // may be null per hop
+    size_t n[kHopMaxGroup];
+    int64_t tile_start[kHopMaxGroup + 1];
+    int64_t staged_end[kHopMaxGroup];          // global tiles below this one are staged (per hop)
+    int count;
+    int local_ready;
+};
+
+template <int FMT, bool REQ_BF16>
+__global__ void __launch_bounds__(kHopThreads)
+ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kHopStages * kHopStageBytes);
+    const int64_t total_tiles = g.tile_start[g.count];
+    const unsigned tid = threadIdx.x;
+    const unsigned lane = tid & 31u, warp = tid >> 5;
+    const unsigned j = lane & 7u, sub = lane >> 3;
+    const unsigned bl = warp * 4 + sub;                    // block inside the tile
+    if (tid == 0) {
+        for (int s = 0; s < kHopStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    auto hop_from = [&](int h, int64_t t) {                // CTA-uniform; t never decreases
+        while (h + 1 < g.count && t >= g.tile_start[h + 1]) ++h;
+        return h;
+    };
+    auto issue_local = [&](int64_t t, int h, int s) {   // thread 0 only
+        const size_t lt = (size_t)(t - g.tile_start[h]);
+        uint8_t* st = smem + (size_t)s * kHopStageBytes;
+        mbar_arrive_expect_tx(&full[s], kHopStageBytes);
+        bulk_g2s(st + kHopCodesBytes + kHopScaleBytes, g.local[h] + lt * kHopTile, kHopLocalBytes, &full[s]);
+    };
+    auto issue_incoming = [&](int64_t t, int h, int s) {   // thread 0 only
+        const size_t lt = (size_t)(t - g.tile_start[h]);
+        uint8_t* st = smem + (size_t)s * kHopStageBytes;
+        bulk_g2s(st, g.in_codes[h] + lt * kHopTile, kHopCodesBytes, &full[s]);
+        bulk_g2s(st + kHopCodesBytes, g.in_scales[h] + lt * kHopTileBlocks, kHopScaleBytes, &full[s]);
+    };
+    // parity / pending as in ring_hop_kernel
+    uint32_t parity = 0, pending = 0;
+    if (tid == 0 && g.local_ready) {
+        int h = 0;
+        for (int s = 0; s < kHopStages; ++s) {
+            const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+            if (t >= total_tiles) break;
+            h = hop_from(h, t);
+            if (t < g.staged_end[h]) {
+                issue_local(t, h, s);
+                pending |= 1u << s;
+            }
+        }
+    }
+    dependency_wait();
+    allow_dependents();
+    __syncthreads();
+    int hp = 0;                                   // thread 0: hop of the next tile to request
+    int64_t tp = blockIdx.x;                      // thread 0: the next tile to request
+    if (tid == 0) {
+        for (int s = 0; s < kHopStages; ++s, tp += gridDim.x) {
+            if (tp >= total_tiles) break;
+            hp = hop_from(hp, tp);
+            if (tp < g.staged_end[hp]) {
+                if (!g.local_ready) issue_local(tp, hp, s);
+                issue_incoming(tp, hp, s);
+                pending |= 1u << s;
+            }
+        }
+    }
+    int s = 0;
+    int h = 0;
+    bool failed = false;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        h = hop_from(h, t);
+        const bool staged = t < g.staged_end[h];
+        const bool ok = staged ? mbar_wait(&full[s], (parity >> s) & 1u) : true;
+        if (staged && ok) {
+            parity ^= 1u << s;
+            pending &= ~(1u << s);
+        }
+        const size_t n = g.n[h];
+        const size_t nb = (n + 127) >> 7;
+        const uint8_t* st = smem + (size_t)s * kHopStageBytes;
+        const size_t b = (size_t)(t - g.tile_start[h]) * kHopTileBlocks + bl;
+        const size_t e0 = (b << 7) + 8 * j;
+        const long long avail = (long long)n - (long long)e0;
+        uint2 ca, cb;
+        uint4 la, lb;
+        float s_in;
+        if (staged) {
+            ca = *reinterpret_cast<const uint2*>(st + bl * 128 + j * 8);
+            cb = *reinterpret_cast<const uint2*>(st + bl * 128 + 64 + j * 8);
+            s_in = *reinterpret_cast<const float*>(st + kHopCodesBytes + bl * 4);
+            const uint8_t* sl = st + kHopCodesBytes + kHopScaleBytes;
+            la = *reinterpret_cast<const uint4*>(sl + bl * 256 + j * 16);
+            lb = *reinterpret_cast<const uint4*>(sl + bl * 256 + 128 + j * 16);
+        } else {
+            ca = ld_u8x8_tail(g.in_codes[h] + e0, avail);
+            cb = ld_u8x8_tail(g.in_codes[h] + e0 + 64, avail - 64);
+            la = ld_bf16x8_tail(g.local[h] + e0, avail);
+            lb = ld_bf16x8_tail(g.local[h] + e0 + 64, avail - 64);
+            s_in = b < nb ? g.in_scales[h][b] : 0.0f;
+        }
+        uint32_t wa[2], wb[2];
+        float y[16];
+        float sc;
+        hop_block16<FMT, REQ_BF16>(ca, cb, la, lb, s_in, wa, wb, y, sc);
+        uint8_t* out_codes = g.out_codes[h];
+        uint16_t* out_bf16 = g.out_bf16[h];
+        if (staged) {
+            st_stream(out_codes + e0, make_uint2(wa[0], wa[1]));
+            st_stream(out_codes + e0 + 64, make_uint2(wb[0], wb[1]));
+            if (j == 0) g.out_scales[h][b] = sc;
+        } else if (b < nb) {
+            st_u8_tail(out_codes + e0, wa, 2, avail);
+            st_u8_tail(out_codes + e0 + 64, wb, 2, avail - 64);
+            if (j == 0) g.out_scales[h][b] = sc;
+        }
+        if (out_bf16 != nullptr) store_hop_bf16(out_bf16, e0, y, staged, b < nb, avail);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        if (tid == 0 && tp < total_tiles) {           // the tile kHopStages ahead, into stage s
+            hp = hop_from(hp, tp);
+            if (tp < g.staged_end[hp]) {
+                fence_proxy_async_smem();
+                issue_local(tp, hp, s);
+                issue_incoming(tp, hp, s);
+                pending |= 1u << s;
+            }
+        }
+        tp += gridDim.x;
+        s = (s + 1 == kHopStages) ? 0 : s + 1;
+    }
+    if (failed && tid == 0) {
+        raise_error(kErrCopyTimeout);
+        for (int q = 0; q < kHopStages; ++q)
+            if (pending & (1u << q)) mbar_wait(&full[q], (parity >> q) & 1u);
+    }
+}
+
 // Host checks of one hop (as documented for fp8q_ring_hop).
 static fp8q_status_t check_hop(const fp8q_hop_t& hp) {
     if (hp.n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
@@ -262,6 +444,16 @@ static void hop_ranges(const fp8q_hop_t& hp, const void* p[6], size_t sz[6]) {
     p[3] = hp.out_codes; sz[3] = n;
     p[4] = hp.out_scales; sz[4] = 4 * nb;
     p[5] = hp.out_bf16;  sz[5] = hp.out_bf16 ? 2 * n : 0;
+}
+
+template <int FMT, bool REQ>
+static fp8q_status_t launch_hop_group_kernel(const HopGroupMulti& g, size_t tiles, cudaStream_t stream) {
+    static KernelCache kc;
+    int resident = 0;
+    const fp8q_status_t st =
+        prepare_kernel(kc, ring_hop_group_kernel<FMT, REQ>, kHopThreads, kHopSmem, kHopSmem, &resident);
+    if (st != FP8Q_OK) return st;
+    return launch(ring_hop_group_kernel<FMT, REQ>, grid_for(tiles, resident), kHopThreads, kHopSmem, stream, g);
 }
 
 template <int FMT, bool REQ>
@@ -302,6 +494,38 @@ static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_
                     if (overlaps(pi[a], si[a], pj[b], sj[b])) return FP8Q_ERR_ALIAS;
                 }
         }
+    }
+    int nonempty = 0;
+    for (int i = 0; i < count; ++i) nonempty += hops[i].n != 0;
+    if (nonempty == 0) return FP8Q_OK;
+    if (nonempty >= 2) {
+        HopGroupMulti g;
+        int used = 0;
+        int64_t start = 0;
+        for (int i = 0; i < count; ++i) {
+            const fp8q_hop_t& hp = hops[i];
+            if (hp.n == 0) continue;
+            g.in_codes[used] = hp.in_codes;
+            g.in_scales[used] = hp.in_scales;
+            g.local[used] = static_cast<const uint16_t*>(hp.local_bf16);
+            g.out_codes[used] = hp.out_codes;
+            g.out_scales[used] = hp.out_scales;
+            g.out_bf16[used] = static_cast<uint16_t*>(hp.out_bf16);
+            g.n[used] = hp.n;
+            g.tile_start[used] = start;
+            g.staged_end[used] = start + (int64_t)(hp.n / kHopTile);
+            start += (int64_t)((hp.n + kHopTile - 1) / kHopTile);
+            ++used;
+        }
+        g.tile_start[used] = start;
+        g.count = used;
+        g.local_ready = (flags & FP8Q_HOP_LOCAL_READY) ? 1 : 0;
+        const size_t tiles = (size_t)start;
+        if (fmt == FP8Q_E4M3)
+            return requant_bf16 ? launch_hop_group_kernel<kE4M3, true>(g, tiles, stream)
+                                : launch_hop_group_kernel<kE4M3, false>(g, tiles, stream);
+        return requant_bf16 ? launch_hop_group_kernel<kE5M2, true>(g, tiles, stream)
+                            : launch_hop_group_kernel<kE5M2, false>(g, tiles, stream);
     }
     HopGroup g;
     int used = 0;
