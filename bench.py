@@ -152,7 +152,8 @@ def measured_peaks():
 
 def kernel_source_hash(name):
     src = {"mxfp8_quantize_kernel": "mxfp8.cu", "quantize_blockwise_kernel": "quantize.cu",
-           "dequant_reduce_kernel": "reduce.cu", "ring_hop_kernel": "ring_hop.cu",
+           "quantize_group_kernel": "quantize.cu", "dequant_reduce_kernel": "reduce.cu",
+           "ring_hop_kernel": "ring_hop.cu", "ring_hop_group_kernel": "ring_hop.cu",
            "mxfp8_dequantize_kernel": "mxfp8_receive.cu", "gather_decode_kernel": "reduce.cu"}[name]
     h = hashlib.sha256()
     for f in (src, "fp8q_device.cuh"):

@@ -274,8 +274,9 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
 // counter.  With several hops the single-hop kernel's per-tile search over
 // the hop table costs about 14% more instructions, in a kernel that is bound
 // by instruction issue at large sizes (8 hops of 16.8M elements: 108.5 us
-// there, 96.3 us here; the 8-rank AllReduce of 256 MiB per rank 1.11 ->
-// 1.03 ms).  For one hop the carried index made the chain slower, so single
+// there, 94.9 us here; the 8-rank AllReduce of 256 MiB per rank 1.07 ->
+// 1.03 ms, with each thread's shared-memory offsets fixed and the outputs
+// addressed from the tile's base).  For one hop the carried index made the chain slower, so single
 // hops keep ring_hop_kernel.
 struct HopGroupMulti {
     const uint8_t* in_codes[kHopMaxGroup];
@@ -301,6 +302,11 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
     const unsigned lane = tid & 31u, warp = tid >> 5;
     const unsigned j = lane & 7u, sub = lane >> 3;
     const unsigned bl = warp * 4 + sub;                    // block inside the tile
+    // this thread's fixed offsets: element (and code byte) inside the tile,
+    // and the shared-memory bytes of its scale and local partial in a stage
+    const unsigned e = bl * 128 + j * 8;
+    const unsigned off_scale = kHopCodesBytes + bl * 4;
+    const unsigned off_local = kHopCodesBytes + kHopScaleBytes + bl * 256 + j * 16;
     if (tid == 0) {
         for (int s = 0; s < kHopStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
@@ -352,6 +358,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
         }
     }
     int s = 0;
+    uint32_t stage_off = 0;
     int h = 0;
     bool failed = false;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
@@ -362,45 +369,49 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
             parity ^= 1u << s;
             pending &= ~(1u << s);
         }
-        const size_t n = g.n[h];
-        const size_t nb = (n + 127) >> 7;
-        const uint8_t* st = smem + (size_t)s * kHopStageBytes;
-        const size_t b = (size_t)(t - g.tile_start[h]) * kHopTileBlocks + bl;
-        const size_t e0 = (b << 7) + 8 * j;
-        const long long avail = (long long)n - (long long)e0;
+        // the tile's first element, and the hop's outputs from there
+        const size_t tile_e = (size_t)(t - g.tile_start[h]) * kHopTile;
+        uint8_t* out_codes = g.out_codes[h] + tile_e;
+        float* out_scales = g.out_scales[h] + tile_e / 128;
+        uint16_t* out_bf16 = g.out_bf16[h];
+        const uint8_t* st = smem + stage_off;
         uint2 ca, cb;
         uint4 la, lb;
         float s_in;
+        long long avail = 0;
+        bool in_range = true;
         if (staged) {
-            ca = *reinterpret_cast<const uint2*>(st + bl * 128 + j * 8);
-            cb = *reinterpret_cast<const uint2*>(st + bl * 128 + 64 + j * 8);
-            s_in = *reinterpret_cast<const float*>(st + kHopCodesBytes + bl * 4);
-            const uint8_t* sl = st + kHopCodesBytes + kHopScaleBytes;
-            la = *reinterpret_cast<const uint4*>(sl + bl * 256 + j * 16);
-            lb = *reinterpret_cast<const uint4*>(sl + bl * 256 + 128 + j * 16);
+            ca = *reinterpret_cast<const uint2*>(st + e);
+            cb = *reinterpret_cast<const uint2*>(st + e + 64);
+            s_in = *reinterpret_cast<const float*>(st + off_scale);
+            la = *reinterpret_cast<const uint4*>(st + off_local);
+            lb = *reinterpret_cast<const uint4*>(st + off_local + 128);
         } else {
+            // the hop's ragged last tile, from global memory
+            const size_t n = g.n[h];
+            const size_t e0 = tile_e + e;
+            avail = (long long)n - (long long)e0;
+            in_range = (e0 >> 7) < ((n + 127) >> 7);
             ca = ld_u8x8_tail(g.in_codes[h] + e0, avail);
             cb = ld_u8x8_tail(g.in_codes[h] + e0 + 64, avail - 64);
             la = ld_bf16x8_tail(g.local[h] + e0, avail);
             lb = ld_bf16x8_tail(g.local[h] + e0 + 64, avail - 64);
-            s_in = b < nb ? g.in_scales[h][b] : 0.0f;
+            s_in = in_range ? g.in_scales[h][e0 >> 7] : 0.0f;
         }
         uint32_t wa[2], wb[2];
         float y[16];
         float sc;
         hop_block16<FMT, REQ_BF16>(ca, cb, la, lb, s_in, wa, wb, y, sc);
-        uint8_t* out_codes = g.out_codes[h];
-        uint16_t* out_bf16 = g.out_bf16[h];
         if (staged) {
-            st_stream(out_codes + e0, make_uint2(wa[0], wa[1]));
-            st_stream(out_codes + e0 + 64, make_uint2(wb[0], wb[1]));
-            if (j == 0) g.out_scales[h][b] = sc;
-        } else if (b < nb) {
-            st_u8_tail(out_codes + e0, wa, 2, avail);
-            st_u8_tail(out_codes + e0 + 64, wb, 2, avail - 64);
-            if (j == 0) g.out_scales[h][b] = sc;
+            st_stream(out_codes + e, make_uint2(wa[0], wa[1]));
+            st_stream(out_codes + e + 64, make_uint2(wb[0], wb[1]));
+            if (j == 0) out_scales[bl] = sc;
+        } else if (in_range) {
+            st_u8_tail(out_codes + e, wa, 2, avail);
+            st_u8_tail(out_codes + e + 64, wb, 2, avail - 64);
+            if (j == 0) out_scales[bl] = sc;
         }
-        if (out_bf16 != nullptr) store_hop_bf16(out_bf16, e0, y, staged, b < nb, avail);
+        if (out_bf16 != nullptr) store_hop_bf16(out_bf16 + tile_e, e, y, staged, in_range, avail);
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
@@ -415,7 +426,13 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
             }
         }
         tp += gridDim.x;
-        s = (s + 1 == kHopStages) ? 0 : s + 1;
+        if (s + 1 == kHopStages) {
+            s = 0;
+            stage_off = 0;
+        } else {
+            ++s;
+            stage_off += kHopStageBytes;
+        }
     }
     if (failed && tid == 0) {
         raise_error(kErrCopyTimeout);
