@@ -46,13 +46,25 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in srcs + hdrs + [__file__])
 
 
+def nvtx_requested() -> bool:
+    """FP8Q_NVTX=1 in the environment compiles the NVTX ranges in (off by default)."""
+    return os.environ.get("FP8Q_NVTX", "0") not in ("", "0")
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
+    stamp = os.path.join(BUILD, "nvtx" if nvtx_requested() else "plain")
+    if not force and up_to_date() and os.path.exists(stamp):
         return LIB
+    if os.path.isdir(BUILD):
+        for f in ("nvtx", "plain"):
+            if os.path.exists(os.path.join(BUILD, f)):
+                os.remove(os.path.join(BUILD, f))
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     srcs, _ = _inputs()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if nvtx_requested():
+        extra += ["-DFP8Q_NVTX=1"]
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
@@ -74,6 +86,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    open(stamp, "w").close()
     return LIB
 
 

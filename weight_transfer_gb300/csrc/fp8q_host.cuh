@@ -11,6 +11,28 @@
 
 #include "fp8q.h"
 
+// Optional NVTX ranges around every entry point that queues GPU work, for
+// timelines in Nsight tools ("FP8 Transmission Optimization for VLA
+// Training", Other Technical Findings: the transfer path was instrumented
+// with NVTX).  Compiled in only when the library is built with FP8Q_NVTX
+// defined (FP8Q_NVTX=1 in the environment of weight_transfer_gb300/build.py);
+// off by default, and then the macro expands to nothing.  NVTX v3 is
+// header-only: without a tool attached a range costs one branch.
+#ifdef FP8Q_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace fp8q {
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace fp8q
+#define FP8Q_NVTX_RANGE(name) ::fp8q::NvtxRange fp8q_nvtx_range_(name)
+#else
+#define FP8Q_NVTX_RANGE(name) ((void)0)
+#endif
+
 namespace fp8q {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

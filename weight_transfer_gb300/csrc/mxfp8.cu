@@ -308,16 +308,19 @@ static fp8q_status_t launch_group(const mxfp8_tensor_t* tensors, int count, cuda
 
 extern "C" fp8q_status_t mxfp8_quantize_swizzled(const void* w_bf16, int64_t batch, int64_t m, int64_t k,
                                                  uint8_t* codes, uint8_t* scales_swizzled, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("mxfp8_quantize_swizzled");
     const mxfp8_tensor_t t = {w_bf16, batch, m, k, codes, scales_swizzled};
     return launch_group(&t, 1, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" fp8q_status_t mxfp8_quantize_swizzled_group(const mxfp8_tensor_t* tensors, int count,
                                                        fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("mxfp8_quantize_swizzled_group");
     return launch_group(tensors, count, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" fp8q_status_t mxfp8_quantize_swizzled_group_ex(const mxfp8_tensor_t* tensors, int count,
                                                           unsigned int flags, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("mxfp8_quantize_swizzled_group_ex");
     return launch_group(tensors, count, reinterpret_cast<cudaStream_t>(stream), flags);
 }

@@ -131,6 +131,7 @@ using namespace fp8q;
 
 extern "C" fp8q_status_t mxfp8_dequantize_swizzled(const uint8_t* codes, const uint8_t* scales_swizzled, int64_t batch,
                                                    int64_t m, int64_t k, void* out_bf16, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("mxfp8_dequantize_swizzled");
     fp8q_status_t st = check_mx_shape(batch, m, k);
     if (st != FP8Q_OK) return st;
     const size_t n = (size_t)batch * (size_t)m * (size_t)k;
@@ -153,6 +154,7 @@ extern "C" fp8q_status_t mxfp8_dequantize_swizzled(const uint8_t* codes, const u
 
 extern "C" fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, int64_t batch, int64_t m, int64_t k,
                                                 uint8_t* scales_rowmajor, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("mxfp8_unswizzle_scales");
     fp8q_status_t st = check_mx_shape(batch, m, k);
     if (st != FP8Q_OK) return st;
     const size_t total = (size_t)batch * (size_t)m * (size_t)(k / MXFP8_BLOCK);
@@ -172,6 +174,7 @@ extern "C" fp8q_status_t mxfp8_unswizzle_scales(const uint8_t* scales_swizzled, 
 
 extern "C" fp8q_status_t fp8q_count_mismatches(const void* a, const void* b, size_t nbytes, unsigned long long* count,
                                                fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_count_mismatches");
     if (nbytes > 16 * FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
     if (nbytes == 0) return FP8Q_OK;
     if (!a || !b || !count) return FP8Q_ERR_NULL;

@@ -103,6 +103,7 @@ extern "C" fp8q_status_t fp8q_pack_plan(const fp8q_pack_item_t* items, int count
 }
 
 extern "C" fp8q_status_t fp8q_copy_segments(const fp8q_copy_t* segs, int count, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_copy_segments");
     if (count < 0 || count > kMaxSegments) return FP8Q_ERR_SIZE;
     if (count == 0) return FP8Q_OK;
     if (!segs) return FP8Q_ERR_NULL;

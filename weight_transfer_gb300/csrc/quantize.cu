@@ -332,17 +332,20 @@ static fp8q_status_t quantize_entry(const void* x_bf16, size_t n, fp8q_format_t 
 
 extern "C" fp8q_status_t fp8q_quantize_blockwise(const void* x_bf16, size_t n, fp8q_format_t fmt,
                                                  uint8_t* codes, float* scales, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_quantize_blockwise");
     return quantize_entry(x_bf16, n, fmt, codes, scales, 0, stream);
 }
 
 extern "C" fp8q_status_t fp8q_quantize_blockwise_ex(const void* x_bf16, size_t n, fp8q_format_t fmt,
                                                     uint8_t* codes, float* scales, unsigned int flags,
                                                     fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_quantize_blockwise_ex");
     return quantize_entry(x_bf16, n, fmt, codes, scales, flags, stream);
 }
 
 extern "C" fp8q_status_t fp8q_encode_f32(const float* x, size_t n, fp8q_format_t fmt, uint8_t* codes,
                                          fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_encode_f32");
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
     if (n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
     if (n == 0) return FP8Q_OK;
@@ -355,6 +358,7 @@ extern "C" fp8q_status_t fp8q_encode_f32(const float* x, size_t n, fp8q_format_t
 
 extern "C" fp8q_status_t fp8q_quantize_blockwise_group(const fp8q_quant_t* items, int count, fp8q_format_t fmt,
                                                        unsigned int flags, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_quantize_blockwise_group");
     if (flags & ~FP8Q_INPUTS_READY) return FP8Q_ERR_FLAGS;
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
     if (!items) return FP8Q_ERR_NULL;

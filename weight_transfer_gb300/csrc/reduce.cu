@@ -357,17 +357,20 @@ static fp8q_status_t reduce_entry(const uint8_t* const* codes, const float* cons
 extern "C" fp8q_status_t fp8q_dequant_reduce(const uint8_t* const* codes, const float* const* scales, int k,
                                              size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
                                              fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_dequant_reduce");
     return reduce_entry(codes, scales, k, n, fmt, out_bf16, out_fp32, 0, stream);
 }
 
 extern "C" fp8q_status_t fp8q_dequant_reduce_ex(const uint8_t* const* codes, const float* const* scales, int k,
                                                 size_t n, fp8q_format_t fmt, void* out_bf16, float* out_fp32,
                                                 unsigned int flags, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_dequant_reduce_ex");
     return reduce_entry(codes, scales, k, n, fmt, out_bf16, out_fp32, flags, stream);
 }
 
 extern "C" fp8q_status_t fp8q_dequantize(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
                                          void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_dequantize");
     ShardPtrs sh;
     const uint8_t* c[1] = {codes};
     const float* sc[1] = {scales};
@@ -520,6 +523,7 @@ fp8q_status_t gather_decode_entry(const uint8_t* codes, const float* scales, siz
 extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes, const float* const* scales,
                                                      int k, size_t n, fp8q_format_t fmt, float* workspace,
                                                      void* out_bf16, float* out_fp32, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_dequant_reduce_unfused");
     ShardPtrs sh;
     fp8q_status_t st = check_shards(codes, scales, k, n, fmt, out_bf16, out_fp32, &sh);
     if (st != FP8Q_OK || n == 0) return st;
@@ -550,6 +554,7 @@ extern "C" fp8q_status_t fp8q_dequant_reduce_unfused(const uint8_t* const* codes
 // ------------------------------------------------- no-allocation variant ----
 extern "C" fp8q_status_t fp8q_gather_decode(const uint8_t* codes, const float* scales, size_t n, fp8q_format_t fmt,
                                             void* const* outs, int count, unsigned int flags, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_gather_decode");
     if (flags & ~FP8Q_ALLREDUCE_MEAN) return FP8Q_ERR_FLAGS;
     return fp8q::gather_decode_entry(codes, scales, n, fmt, outs, count, (flags & FP8Q_ALLREDUCE_MEAN) ? count : 0,
                                      stream);
@@ -589,6 +594,7 @@ static fp8q_status_t static_scratch_address(float** out) {
 extern "C" fp8q_status_t fp8q_dequant_reduce_unfused_static(const uint8_t* const* codes, const float* const* scales,
                                                             int k, size_t n, fp8q_format_t fmt, void* out_bf16,
                                                             float* out_fp32, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_dequant_reduce_unfused_static");
     ShardPtrs sh;
     fp8q_status_t st = check_shards(codes, scales, k, n, fmt, out_bf16, out_fp32, &sh);
     if (st != FP8Q_OK || n == 0) return st;

@@ -58,6 +58,7 @@ extern "C" fp8q_status_t fp8q_ring_allreduce_sim_ex(const void* const* partials,
                                                     size_t n, fp8q_format_t fmt, void* workspace,
                                                     size_t workspace_bytes, uint64_t* wire_bytes, unsigned int flags,
                                                     fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_ring_allreduce_sim_ex");
     using namespace fp8q;
     if (flags & ~FP8Q_ALLREDUCE_MEAN) return FP8Q_ERR_FLAGS;
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
@@ -146,6 +147,7 @@ extern "C" fp8q_status_t fp8q_ring_allreduce_sim(const void* const* partials, vo
                                                  size_t n, fp8q_format_t fmt, void* workspace,
                                                  size_t workspace_bytes, uint64_t* wire_bytes,
                                                  fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_ring_allreduce_sim");
     return fp8q_ring_allreduce_sim_ex(partials, results, ranks, n, fmt, workspace, workspace_bytes, wire_bytes, 0u,
                                       stream);
 }

@@ -584,17 +584,20 @@ using namespace fp8q;
 extern "C" fp8q_status_t fp8q_ring_hop(const uint8_t* in_codes, const float* in_scales, const void* local_bf16,
                                        size_t n, fp8q_format_t fmt, uint8_t* out_codes, float* out_scales,
                                        void* out_bf16, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_ring_hop");
     const fp8q_hop_t hp = {in_codes, in_scales, local_bf16, n, out_codes, out_scales, out_bf16};
     return launch_hops(&hp, 1, fmt, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" fp8q_status_t fp8q_ring_hop_group(const fp8q_hop_t* hops, int count, fp8q_format_t fmt,
                                              fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_ring_hop_group");
     return launch_hops(hops, count, fmt, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" fp8q_status_t fp8q_ring_hop_group_ex(const fp8q_hop_t* hops, int count, fp8q_format_t fmt,
                                                 unsigned int flags, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_ring_hop_group_ex");
     return launch_hops(hops, count, fmt, reinterpret_cast<cudaStream_t>(stream), false, flags);
 }
 
@@ -602,6 +605,7 @@ extern "C" fp8q_status_t fp8q_ring_hop_bf16_requant(const uint8_t* in_codes, con
                                                     const void* local_bf16, size_t n, fp8q_format_t fmt,
                                                     uint8_t* out_codes, float* out_scales, void* out_bf16,
                                                     fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_ring_hop_bf16_requant");
     const fp8q_hop_t hp = {in_codes, in_scales, local_bf16, n, out_codes, out_scales, out_bf16};
     return launch_hops(&hp, 1, fmt, reinterpret_cast<cudaStream_t>(stream), true);
 }

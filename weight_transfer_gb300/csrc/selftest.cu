@@ -47,6 +47,7 @@ unsigned unit_errors_selftest(bool clear) { return read_unit_errors(clear); }
 
 extern "C" fp8q_status_t fp8q_selftest_copy_wait(const void* src, void* dst, uint64_t limit_ns,
                                                  fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_selftest_copy_wait");
     using namespace fp8q;
     if ((src == nullptr) != (dst == nullptr)) return FP8Q_ERR_NULL;
     if (src != nullptr && (!aligned16(src) || !aligned16(dst))) return FP8Q_ERR_ALIGN;

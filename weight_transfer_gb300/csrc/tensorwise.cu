@@ -104,6 +104,7 @@ using namespace fp8q;
 
 extern "C" fp8q_status_t fp8q_quantize_tensorwise(const void* x_bf16, size_t n, fp8q_format_t fmt, uint8_t* codes,
                                                   float* scale_amax, fp8q_stream_t stream) {
+    FP8Q_NVTX_RANGE("fp8q_quantize_tensorwise");
     if (!valid_fmt(fmt)) return FP8Q_ERR_FORMAT;
     if (n > FP8Q_MAX_ELEMENTS) return FP8Q_ERR_SIZE;
     if (n == 0) return FP8Q_OK;
