@@ -31,8 +31,11 @@ def run_quant(w, xbits, fmt):
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
-@pytest.mark.parametrize("n", [1, 7, 8, 9, 127, 128, 129, 255, 256, 300, 4096 + 17, 128 * 1000 + 77, 1 << 20])
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 127, 128, 129, 255, 256, 300, 4096 + 17, 128 * 1000 + 77, 1 << 20,
+                               8192 * 2 + 5, 8192 * 5, 8192 * 7 + 8191])
 def test_quantize_sizes(w, orc, fmt, n):
+    # each CTA takes two consecutive 8192-element tiles: an odd tile count
+    # leaves the last CTA one tile, staged (8192 * 5) or ragged (8192 * 2 + 5)
     xb = varied_bf16(n, seed=n + 31 * fmt)
     codes, scales = run_quant(w, xb, fmt)
     oc, os_ = orc.quantize_blockwise(xb, fmt)

@@ -76,6 +76,38 @@ __device__ __forceinline__ int group_of(const MxGroup& g, int64_t t) {
     return gi;
 }
 
+// Where one tile of the group lives: its tensor, matrix, row and column
+// tile, and its outputs.  Both of a CTA's tiles are resolved first, before
+// anything waits, so the parameter loads overlap the copies in flight
+// (264 us against 268 us for the layer when they were resolved after each
+// tile's data had landed).
+struct MxTileDesc {
+    const CUtensorMap* tmap;
+    uint8_t* codes;
+    uint8_t* scales_tile;
+    int64_t m, k, bt, rt, ct;
+    int y;       // tensor-map row coordinate
+    bool valid;
+};
+
+__device__ __forceinline__ MxTileDesc mx_desc(const MxGroup& g, int64_t t, int64_t total_tiles) {
+    MxTileDesc d;
+    d.valid = t < total_tiles;
+    const int gi = group_of(g, d.valid ? t : 0);
+    const int64_t local = t - g.tile_start[gi];
+    d.m = g.m[gi];
+    d.k = g.k[gi];
+    d.bt = local / g.tiles_per_mat[gi];
+    const int64_t rem = local - d.bt * g.tiles_per_mat[gi];
+    d.rt = rem / g.col_tiles[gi];
+    d.ct = rem - d.rt * g.col_tiles[gi];
+    d.tmap = &g.tmap[gi];
+    d.codes = g.codes[gi];
+    d.scales_tile = g.scales[gi] + local * 512;
+    d.y = (int)(d.bt * d.m + d.rt * 128);
+    return d;
+}
+
 __global__ void __launch_bounds__(kMxThreads)
 mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -89,24 +121,22 @@ mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
     const unsigned jl = c >> 2;                    // scale column inside the tile
     const int64_t total_tiles = g.tile_start[g.count];
     const int64_t t0 = (int64_t)blockIdx.x * kMxTilesPerCta;
+    // both tiles' coordinates, resolved before anything waits
+    const MxTileDesc D0 = mx_desc(g, t0, total_tiles);
+    const MxTileDesc D1 = mx_desc(g, t0 + 1, total_tiles);
 
     if (tid == 0) {
         for (int s = 0; s < kMxTilesPerCta; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
-    auto request = [&]() {                        // thread 0 only: both tiles
-        for (int s = 0; s < kMxTilesPerCta; ++s) {
-            const int64_t t = t0 + s;
-            if (t >= total_tiles) break;
-            const int gi = group_of(g, t);
-            const int64_t local = t - g.tile_start[gi];
-            const int64_t bt = local / g.tiles_per_mat[gi];
-            const int64_t rem = local - bt * g.tiles_per_mat[gi];
-            const int64_t rt = rem / g.col_tiles[gi];
-            const int64_t ct = rem - rt * g.col_tiles[gi];
-            mbar_arrive_expect_tx(&full[s], kMxStageBytes);
-            tma_2d_g2s(smem + (size_t)s * kMxStageBytes, &g.tmap[gi], (int)(ct * 128),
-                       (int)(bt * g.m[gi] + rt * 128), &full[s]);
+    auto request = [&]() {
+        if (D0.valid) {
+            mbar_arrive_expect_tx(&full[0], kMxStageBytes);
+            tma_2d_g2s(smem, D0.tmap, (int)(D0.ct * 128), D0.y, &full[0]);
+        }
+        if (D1.valid) {
+            mbar_arrive_expect_tx(&full[1], kMxStageBytes);
+            tma_2d_g2s(smem + kMxStageBytes, D1.tmap, (int)(D1.ct * 128), D1.y, &full[1]);
         }
     };
     // with inputs_ready the caller guarantees that no kernel still running
@@ -119,26 +149,20 @@ mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
 
     int it = 0;
     bool failed = false;
+#pragma unroll
     for (; it < kMxTilesPerCta; ++it) {
-        const int64_t t = t0 + it;
-        if (t >= total_tiles) break;
+        const MxTileDesc& D = it == 0 ? D0 : D1;
+        if (!D.valid) break;
         const bool ok = mbar_wait(&full[it], 0u);
         const uint8_t* st = smem + (size_t)it * kMxStageBytes;
         uint8_t* sb = sbuf + (it & 1) * 512;
-        const int gi = group_of(g, t);
-        const int64_t m = g.m[gi], k = g.k[gi];
-        const int64_t local = t - g.tile_start[gi];
-        const int64_t bt = local / g.tiles_per_mat[gi];
-        const int64_t rem = local - bt * g.tiles_per_mat[gi];
-        const int64_t rt = rem / g.col_tiles[gi];
-        const int64_t ct = rem - rt * g.col_tiles[gi];
-        const int64_t col = ct * 128 + c * 8;
+        const int64_t m = D.m, k = D.k;
+        const int64_t col = D.ct * 128 + c * 8;
         const bool col_ok = col < k;
-        uint8_t* codes = g.codes[gi];
 #pragma unroll
         for (int i = 0; i < kMxRowsPerWarp / 2; ++i) {
             const int rl = warp * kMxRowsPerWarp + 2 * i + (lane >> 4);    // row inside the tile
-            const int64_t row = rt * 128 + rl;
+            const int64_t row = D.rt * 128 + rl;
             const uint4 v = *reinterpret_cast<const uint4*>(st + rl * 256 + c * 16);
             float f[8];
             unpack8(v, f);
@@ -155,7 +179,7 @@ mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) q[e] = __fmul_rn(f[e], factor);
             if (valid)
-                st_stream(codes + ((bt * m + row) * k + col),
+                st_stream(D.codes + ((D.bt * m + row) * k + col),
                           make_uint2(cvt_fp8x4<kE4M3>(q[0], q[1], q[2], q[3]), cvt_fp8x4<kE4M3>(q[4], q[5], q[6], q[7])));
             if ((c & 3u) == 0) sb[(rl & 31) * 16 + (rl >> 5) * 4 + jl] = (uint8_t)e8;
         }
@@ -163,7 +187,7 @@ mxfp8_quantize_kernel(const __grid_constant__ MxGroup g) {
             failed = true;
             break;
         }
-        if (tid < 32) st_stream(g.scales[gi] + local * 512 + tid * 16, *reinterpret_cast<const uint4*>(sb + tid * 16));
+        if (tid < 32) st_stream(D.scales_tile + tid * 16, *reinterpret_cast<const uint4*>(sb + tid * 16));
     }
     if (failed && tid == 0) {
         // report, and let the copies still in flight land before the CTA's
