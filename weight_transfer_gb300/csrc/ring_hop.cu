@@ -9,7 +9,8 @@
 // is reduced, nothing is re-read from HBM.
 //
 // Work split: a persistent CTA of 256 threads walks tiles of 32 blocks
-// (4096 elements).  Thread 0 keeps up to kHopStages tiles in flight; a tile
+// (4096 elements).  Thread 0 keeps up to 3 tiles in flight (2 on short
+// hops, see launch_hop_kernel); a tile
 // is three bulk copies into one shared-memory stage (4096 incoming codes,
 // their 32 scales, 8 KB of the local bf16 partial) armed on the stage's
 // mbarrier.  Once it has landed, 8 lanes own one block: lane j takes
@@ -118,11 +119,13 @@ __device__ __forceinline__ void store_hop_bf16(uint16_t* out_bf16, size_t e0, co
     }
 }
 
-template <int FMT, bool REQ_BF16>
+// NST stages of kHopStageBytes each (2 for short hops, 3 otherwise; see
+// launch_hop_kernel).
+template <int FMT, bool REQ_BF16, int NST>
 __global__ void __launch_bounds__(kHopThreads)
 ring_hop_kernel(const __grid_constant__ HopGroup g) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kHopStages * kHopStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * kHopStageBytes);
     const int64_t total_tiles = g.tile_start[g.count];
     const unsigned tid = threadIdx.x;
     const unsigned lane = tid & 31u, warp = tid >> 5;
@@ -135,7 +138,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
         return h;
     };
     if (tid == 0) {
-        for (int s = 0; s < kHopStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
     // a tile is staged through shared memory when it lies entirely inside its hop's arrays
@@ -164,7 +167,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
     // the first tiles' local partials, before the predecessor grid has ended,
     // when the caller guarantees that it does not write them
     if (tid == 0 && g.local_ready)
-        for (int s = 0; s < kHopStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
             if (t < total_tiles) {
                 const int h = hop_of(t);
@@ -178,7 +181,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
     allow_dependents();
     __syncthreads();
     if (tid == 0)
-        for (int s = 0; s < kHopStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
             if (t < total_tiles) {
                 const int h = hop_of(t);
@@ -193,7 +196,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
     int it = 0;
     bool failed = false;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
-        const int s = it % kHopStages;
+        const int s = it % NST;
         const int h = hop_of(t);
         const size_t n = g.n[h];
         const bool staged = staged_tile(t, h);
@@ -246,7 +249,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
             break;
         }
         if (tid == 0) {
-            const int64_t tn = t + (int64_t)kHopStages * gridDim.x;     // next tile of stage s
+            const int64_t tn = t + (int64_t)NST * gridDim.x;     // next tile of stage s
             if (tn < total_tiles) {
                 const int hn = hop_of(tn);
                 if (staged_tile(tn, hn)) {
@@ -262,7 +265,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
         // report, and let the copies still in flight land before the CTA's
         // shared memory is released
         raise_error(kErrCopyTimeout);
-        for (int s = 0; s < kHopStages; ++s)
+        for (int s = 0; s < NST; ++s)
             if (pending & (1u << s)) mbar_wait(&full[s], (parity >> s) & 1u);
     }
 }
@@ -473,13 +476,25 @@ static fp8q_status_t launch_hop_group_kernel(const HopGroupMulti& g, size_t tile
     return launch(ring_hop_group_kernel<FMT, REQ>, grid_for(tiles, resident), kHopThreads, kHopSmem, stream, g);
 }
 
+template <int FMT, bool REQ, int NST>
+static fp8q_status_t launch_hop_kernel_n(const HopGroup& g, size_t tiles, cudaStream_t stream) {
+    static KernelCache kc;
+    constexpr size_t smem = (size_t)NST * kHopStageBytes + 8 * NST;
+    int resident = 0;
+    const fp8q_status_t st = prepare_kernel(kc, ring_hop_kernel<FMT, REQ, NST>, kHopThreads, smem, smem, &resident);
+    if (st != FP8Q_OK) return st;
+    return launch(ring_hop_kernel<FMT, REQ, NST>, grid_for(tiles, resident), kHopThreads, smem, stream, g);
+}
+
+// A short hop (under 8 tiles per CTA of a full persistent grid, e.g. the
+// 13.1M-element shard: 3,200 tiles over 608 CTAs) is ramp-up and tail, and
+// 2 stages start it sooner (the 7-hop chain at 13.1M: 75.0 against 77.0 us);
+// a long one needs the third stage's bytes in flight (64 MiB per hop: 170.5
+// against 173.0 us).
 template <int FMT, bool REQ>
 static fp8q_status_t launch_hop_kernel(const HopGroup& g, size_t tiles, cudaStream_t stream) {
-    static KernelCache kc;
-    int resident = 0;
-    const fp8q_status_t st = prepare_kernel(kc, ring_hop_kernel<FMT, REQ>, kHopThreads, kHopSmem, kHopSmem, &resident);
-    if (st != FP8Q_OK) return st;
-    return launch(ring_hop_kernel<FMT, REQ>, grid_for(tiles, resident), kHopThreads, kHopSmem, stream, g);
+    if (tiles < (size_t)8 * 4 * (size_t)sm_count()) return launch_hop_kernel_n<FMT, REQ, 2>(g, tiles, stream);
+    return launch_hop_kernel_n<FMT, REQ, 3>(g, tiles, stream);
 }
 
 static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_t fmt, cudaStream_t stream,
