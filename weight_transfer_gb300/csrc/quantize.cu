@@ -300,6 +300,7 @@ static fp8q_status_t launch_quantize_group(const QuantGroup& g, size_t tiles, cu
                                             &resident);
     if (st != FP8Q_OK) return st;
     const size_t grid = (tiles + kQuantTilesPerCta - 1) / kQuantTilesPerCta;
+    if (grid > 0x7FFFFFFFu) return FP8Q_ERR_SIZE;        // beyond the grid limit (about 2^44 elements)
     return launch(quantize_group_kernel<FMT>, (unsigned)grid, kQuantThreads, kQuantSmem, stream, g);
 }
 
