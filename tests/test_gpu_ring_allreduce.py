@@ -151,3 +151,28 @@ def test_gather_decode_matches_oracle(w, orc, fmt, count, n, mean):
     want, _ = orc.dequantize_mean(codes[0], sc, fmt, count) if mean else orc.dequantize(codes[0], sc, fmt)
     for o, t in enumerate(outs):
         assert_same(bits16(t), want, f"output {o}")
+
+
+@pytest.mark.parametrize("mean", [False, True])
+def test_ring_allreduce_256mib_per_rank_sampled(w, orc, mean):
+    # the bench's large configuration, 8 ranks x 2^27 elements (256 MiB of
+    # bf16 per rank), checked on sampled outputs: the result at a position
+    # depends only on that position's 128-block in every rank, through the
+    # same ring schedule for its chunk, so the oracle's AllReduce of the
+    # sampled pieces (piece c taken from chunk c) gives those outputs exactly
+    P, n = 8, 8 * (1 << 24)
+    m, L = n // P, 1 << 16
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    parts = [torch.randn(n, device="cuda", generator=g).mul_(1e-4).to(torch.bfloat16) for _ in range(P)]
+    res, _ = w.fp8q_ring_allreduce_sim(parts, "e4m3", mean=mean)
+    torch.cuda.synchronize()
+    for off in (0, m // 2 + 128 * 37, m - L):
+        idx = torch.cat([torch.arange(c * m + off, c * m + off + L, device="cuda") for c in range(P)])
+        sub = [bits16(p[idx]) for p in parts]
+        want = oracle_allreduce(orc, sub, 0, mean)
+        for r in (0, 3, P - 1):
+            assert_same(bits16(res[r][idx]), want, f"rank {r}, offset {off}")
+        del idx
+    del parts, res
+    torch.cuda.empty_cache()
