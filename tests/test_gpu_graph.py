@@ -124,3 +124,38 @@ def test_captured_step_replays_like_eager_and_oracle(w, orc):
             ec, es = orc.mxfp8_quantize_swizzled(bits16(st.mx_in[i]).ravel(), bb, m, k)
             assert_same(u8(st.mx_c[i]).ravel(), ec, f"mxfp8 codes {i}")
             assert_same(st.mx_s[i].cpu().numpy()[:es.size], es, f"mxfp8 scales {i}")
+
+
+def test_captured_ring_allreduce_replays_like_eager_and_oracle(w, orc):
+    # the simulated AllReduce (one grouped quantize, 7 grouped hops, the
+    # all-gather decode: 9 launches from one C call) captured once, replayed
+    # on new partials written in place; with and without the mean
+    from test_gpu_ring_allreduce import oracle_allreduce
+    P, n = 8, 8 * 512 * 11
+    parts = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    res = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    ws = torch.empty(int(w.lib().fp8q_ring_allreduce_workspace_bytes(P, n)), dtype=torch.uint8, device="cuda")
+    for mean in (False, True):
+        def fill(seed):
+            for r in range(P):
+                parts[r].copy_(gen.normal_bf16(n, 1e-3, seed=seed + r, outlier_p=1e-3, outlier_mult=100.0))
+        fill(10)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):        # first-call setup outside capture
+            w.fp8q_ring_allreduce_sim(parts, "e4m3", results=res, workspace=ws, mean=mean)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            w.fp8q_ring_allreduce_sim(parts, "e4m3", results=res, workspace=ws, mean=mean)
+        for seed in (20, 30):
+            fill(seed)
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            got = [bits16(r) for r in res]
+            want = oracle_allreduce(orc, [bits16(p) for p in parts], 0, mean)
+            for r in range(P):
+                assert_same(got[r], want, f"rank {r}, seed {seed}, mean {mean}")
+        del g
