@@ -42,8 +42,6 @@ constexpr int kHopCodesBytes = kHopTile;
 constexpr int kHopScaleBytes = 4 * kHopTileBlocks;
 constexpr int kHopLocalBytes = 2 * kHopTile;
 constexpr int kHopStageBytes = kHopCodesBytes + kHopScaleBytes + kHopLocalBytes;
-constexpr int kHopStages = 3;
-constexpr size_t kHopSmem = (size_t)kHopStages * kHopStageBytes + 8 * kHopStages;
 
 // Up to kHopMaxGroup independent hops in one launch (all ranks' hops of one
 // step of a ring simulated on one GPU).  Hop h owns the global tiles
@@ -295,11 +293,11 @@ struct HopGroupMulti {
     int local_ready;
 };
 
-template <int FMT, bool REQ_BF16>
+template <int FMT, bool REQ_BF16, int NST>
 __global__ void __launch_bounds__(kHopThreads)
 ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kHopStages * kHopStageBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * kHopStageBytes);
     const int64_t total_tiles = g.tile_start[g.count];
     const unsigned tid = threadIdx.x;
     const unsigned lane = tid & 31u, warp = tid >> 5;
@@ -311,7 +309,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
     const unsigned off_scale = kHopCodesBytes + bl * 4;
     const unsigned off_local = kHopCodesBytes + kHopScaleBytes + bl * 256 + j * 16;
     if (tid == 0) {
-        for (int s = 0; s < kHopStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
     }
     auto hop_from = [&](int h, int64_t t) {                // CTA-uniform; t never decreases
@@ -334,7 +332,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
     uint32_t parity = 0, pending = 0;
     if (tid == 0 && g.local_ready) {
         int h = 0;
-        for (int s = 0; s < kHopStages; ++s) {
+        for (int s = 0; s < NST; ++s) {
             const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
             if (t >= total_tiles) break;
             h = hop_from(h, t);
@@ -350,7 +348,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
     int hp = 0;                                   // thread 0: hop of the next tile to request
     int64_t tp = blockIdx.x;                      // thread 0: the next tile to request
     if (tid == 0) {
-        for (int s = 0; s < kHopStages; ++s, tp += gridDim.x) {
+        for (int s = 0; s < NST; ++s, tp += gridDim.x) {
             if (tp >= total_tiles) break;
             hp = hop_from(hp, tp);
             if (tp < g.staged_end[hp]) {
@@ -419,7 +417,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
             failed = true;
             break;
         }
-        if (tid == 0 && tp < total_tiles) {           // the tile kHopStages ahead, into stage s
+        if (tid == 0 && tp < total_tiles) {           // the tile NST ahead, into stage s
             hp = hop_from(hp, tp);
             if (tp < g.staged_end[hp]) {
                 fence_proxy_async_smem();
@@ -429,7 +427,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
             }
         }
         tp += gridDim.x;
-        if (s + 1 == kHopStages) {
+        if (s + 1 == NST) {
             s = 0;
             stage_off = 0;
         } else {
@@ -439,7 +437,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
     }
     if (failed && tid == 0) {
         raise_error(kErrCopyTimeout);
-        for (int q = 0; q < kHopStages; ++q)
+        for (int q = 0; q < NST; ++q)
             if (pending & (1u << q)) mbar_wait(&full[q], (parity >> q) & 1u);
     }
 }
@@ -466,14 +464,22 @@ static void hop_ranges(const fp8q_hop_t& hp, const void* p[6], size_t sz[6]) {
     p[5] = hp.out_bf16;  sz[5] = hp.out_bf16 ? 2 * n : 0;
 }
 
-template <int FMT, bool REQ>
-static fp8q_status_t launch_hop_group_kernel(const HopGroupMulti& g, size_t tiles, cudaStream_t stream) {
+template <int FMT, bool REQ, int NST>
+static fp8q_status_t launch_hop_group_kernel_n(const HopGroupMulti& g, size_t tiles, cudaStream_t stream) {
     static KernelCache kc;
+    constexpr size_t smem = (size_t)NST * kHopStageBytes + 8 * NST;
     int resident = 0;
     const fp8q_status_t st =
-        prepare_kernel(kc, ring_hop_group_kernel<FMT, REQ>, kHopThreads, kHopSmem, kHopSmem, &resident);
+        prepare_kernel(kc, ring_hop_group_kernel<FMT, REQ, NST>, kHopThreads, smem, smem, &resident);
     if (st != FP8Q_OK) return st;
-    return launch(ring_hop_group_kernel<FMT, REQ>, grid_for(tiles, resident), kHopThreads, kHopSmem, stream, g);
+    return launch(ring_hop_group_kernel<FMT, REQ, NST>, grid_for(tiles, resident), kHopThreads, smem, stream, g);
+}
+
+// The stage count as for single hops (see launch_hop_kernel).
+template <int FMT, bool REQ>
+static fp8q_status_t launch_hop_group_kernel(const HopGroupMulti& g, size_t tiles, cudaStream_t stream) {
+    if (tiles < (size_t)8 * 4 * (size_t)sm_count()) return launch_hop_group_kernel_n<FMT, REQ, 2>(g, tiles, stream);
+    return launch_hop_group_kernel_n<FMT, REQ, 3>(g, tiles, stream);
 }
 
 template <int FMT, bool REQ, int NST>
