@@ -18,8 +18,10 @@ def w():
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
-@pytest.mark.parametrize("n", [1, 7, 128, 129, 4096 + 17, 1 << 20])
+@pytest.mark.parametrize("n", [1, 7, 128, 129, 4096 + 17, 1 << 20, 8192 * 3, 8192 * 2 + 9, 8192 * 5 + 8191])
 def test_tensorwise_random(w, orc, fmt, n):
+    # two 8192-element tiles per CTA: odd tile counts leave the last CTA one
+    # tile, staged or ragged
     rng = np.random.default_rng(n + fmt)
     x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-20, 20)).astype(np.float32)
     x[rng.random(n) < 0.001] *= 300.0

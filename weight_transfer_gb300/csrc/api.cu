@@ -68,6 +68,6 @@ extern "C" fp8q_status_t fp8q_device_errors(unsigned int* flags, int clear) {
     if (e != cudaSuccess) return fp8q::cuda_status(e);
     *flags = fp8q::unit_errors_quantize(clear != 0) | fp8q::unit_errors_reduce(clear != 0) |
              fp8q::unit_errors_ring_hop(clear != 0) | fp8q::unit_errors_mxfp8(clear != 0) |
-             fp8q::unit_errors_selftest(clear != 0);
+             fp8q::unit_errors_selftest(clear != 0) | fp8q::unit_errors_tensorwise(clear != 0);
     return FP8Q_OK;
 }

@@ -59,6 +59,7 @@ unsigned unit_errors_reduce(bool clear);
 unsigned unit_errors_ring_hop(bool clear);
 unsigned unit_errors_mxfp8(bool clear);
 unsigned unit_errors_selftest(bool clear);
+unsigned unit_errors_tensorwise(bool clear);
 
 // Devices whose per-device state is cached; others are set up on every call.
 constexpr int kMaxDevices = 64;

@@ -7,13 +7,26 @@
 // block spanning all n elements:
 //   amax = max |x_i|,  s = RN(amax / Fmax),  c_i = satfinite RNE_fp8(RN(x_i / s)).
 // Two passes over x: an amax kernel (bf16 magnitudes compared as integers,
-// which orders them exactly; one atomicMax per warp) and an encode kernel
+// which orders them exactly; one atomicMax per CTA) and an encode kernel
 // that derives s from the amax and converts with the per-tensor reciprocal
 // and one Markstein step (exact for bf16 dividends, see block_quotients).
+// Both stage their tiles with bulk copies on one-pass grids, like the
+// blockwise quantizer (the earlier register-load grid-stride kernels took
+// about 85-88 us on the 8 x 13.1M bucket).
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
 namespace fp8q {
+
+// Both passes stage tiles of 8192 elements (16 KB of bf16) with one bulk
+// copy each, two consecutive tiles per CTA of 256 threads on a grid that
+// covers the tensor once -- the blockwise quantizer's layout.  A tile's
+// ragged end is read from global memory with guarded loads.
+constexpr int kTwThreads = 256;
+constexpr int kTwTile = 8192;
+constexpr int kTwStageBytes = 2 * kTwTile;
+constexpr int kTwTilesPerCta = 2;
+constexpr size_t kTwSmem = (size_t)kTwTilesPerCta * kTwStageBytes + 8 * kTwTilesPerCta;
 
 // Largest bf16 magnitude bits among the 8 elements of v.
 __device__ __forceinline__ uint32_t amax_bits8(const uint4& v, uint32_t m) {
@@ -23,61 +36,136 @@ __device__ __forceinline__ uint32_t amax_bits8(const uint4& v, uint32_t m) {
     return m;
 }
 
-// scale_amax[1] accumulates the amax as binary32 bits (non-negative floats
-// order like their bit patterns).  Each thread keeps four 16-byte loads in
-// flight: with one, the loads a GPU can hold in flight do not cover HBM's
-// latency at full bandwidth.
-__global__ void __launch_bounds__(256)
-tensor_amax_kernel(const uint16_t* __restrict__ x, size_t n, float* scale_amax) {
-    dependency_wait();
-    allow_dependents();
-    uint32_t m = 0;
-    const size_t n8 = n / 8;
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    size_t i = t0;
-    for (; i + 3 * stride < n8; i += 4 * stride) {
-        const uint4 v0 = ld_stream(x + 8 * i);
-        const uint4 v1 = ld_stream(x + 8 * (i + stride));
-        const uint4 v2 = ld_stream(x + 8 * (i + 2 * stride));
-        const uint4 v3 = ld_stream(x + 8 * (i + 3 * stride));
-        m = amax_bits8(v3, amax_bits8(v2, amax_bits8(v1, amax_bits8(v0, m))));
+// The CTA's two tiles requested into their stages (thread 0); returns the
+// number of tiles the CTA owns.
+__device__ __forceinline__ int tw_request(const uint16_t* x, size_t n, uint8_t* smem, uint64_t* full, size_t t0) {
+    const size_t nstaged = n / kTwTile;
+    int owned = 0;
+    for (int s = 0; s < kTwTilesPerCta; ++s) {
+        const size_t t = t0 + s;
+        if (t * kTwTile >= n) break;
+        owned = s + 1;
+        if (threadIdx.x == 0 && t < nstaged) {
+            mbar_arrive_expect_tx(&full[s], kTwStageBytes);
+            bulk_g2s(smem + (size_t)s * kTwStageBytes, x + t * kTwTile, kTwStageBytes, &full[s]);
+        }
     }
-    for (; i < n8; i += stride) m = amax_bits8(ld_stream(x + 8 * i), m);
-    for (size_t i = 8 * n8 + t0; i < n; i += stride) m = max(m, (uint32_t)(x[i] & 0x7FFFu));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if ((threadIdx.x & 31u) == 0 && m) atomicMax(reinterpret_cast<unsigned*>(scale_amax) + 1, m << 16);
+    return owned;
 }
 
-template <int FMT>
-__global__ void __launch_bounds__(256)
-tensor_encode_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __restrict__ codes, float* scale_amax) {
+// Round r of a tile: this thread's 8 elements [e, e + 8) of the tile,
+// e = r * 2048 + 8 * tid, from shared memory or (ragged tile) global memory.
+__device__ __forceinline__ uint4 tw_load8(const uint8_t* st, bool staged, const uint16_t* x, size_t n, size_t t,
+                                          unsigned e) {
+    if (staged) return *reinterpret_cast<const uint4*>(st + 2 * e);
+    const size_t g = t * kTwTile + e;
+    return ld_bf16x8_tail(x + g, (long long)n - (long long)g);
+}
+
+// scale_amax[1] accumulates the amax as binary32 bits (non-negative floats
+// order like their bit patterns): one atomicMax per CTA.
+__global__ void __launch_bounds__(kTwThreads)
+tensor_amax_kernel(const uint16_t* __restrict__ x, size_t n, float* scale_amax) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint32_t warp_max[kTwThreads / 32];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTwTilesPerCta * kTwStageBytes);
+    const size_t t0 = (size_t)blockIdx.x * kTwTilesPerCta;
+    const size_t nstaged = n / kTwTile;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTwTilesPerCta; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
     dependency_wait();
     allow_dependents();
+    __syncthreads();
+    const int owned = tw_request(x, n, smem, full, t0);
+    uint32_t m = 0;
+    bool ok = true;
+    int s = 0;
+    for (; s < owned; ++s) {
+        const size_t t = t0 + s;
+        const bool staged = t < nstaged;
+        if (staged && !mbar_wait(&full[s], 0u)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* st = smem + (size_t)s * kTwStageBytes;
+#pragma unroll
+        for (int r = 0; r < kTwTile / (8 * kTwThreads); ++r)
+            m = amax_bits8(tw_load8(st, staged, x, n, t, r * 8 * kTwThreads + 8 * threadIdx.x), m);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31u) == 0) warp_max[threadIdx.x >> 5] = m;
+    if (__syncthreads_or(!ok)) {
+        if (threadIdx.x == 0) {
+            raise_error(kErrCopyTimeout);
+            for (int r = s; r < owned; ++r)
+                if (t0 + r < nstaged) mbar_wait(&full[r], 0u);
+        }
+        return;
+    }
+    if (threadIdx.x == 0) {
+        uint32_t c = 0;
+        for (int i = 0; i < kTwThreads / 32; ++i) c = max(c, warp_max[i]);
+        if (c) atomicMax(reinterpret_cast<unsigned*>(scale_amax) + 1, c << 16);
+    }
+}
+
+// s from the amax (as the blockwise scale), then each element's code with
+// the tensor's reciprocal and one Markstein step (exact for bf16 dividends,
+// see block_quotients).
+template <int FMT>
+__global__ void __launch_bounds__(kTwThreads)
+tensor_encode_kernel(const uint16_t* __restrict__ x, size_t n, uint8_t* __restrict__ codes, float* scale_amax) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTwTilesPerCta * kTwStageBytes);
+    const size_t t0 = (size_t)blockIdx.x * kTwTilesPerCta;
+    const size_t nstaged = n / kTwTile;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTwTilesPerCta; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    // x is an input of the whole call, and the amax kernel before this one
+    // does not write it: the tiles may be requested before the wait
+    const int owned = tw_request(x, n, smem, full, t0);
+    dependency_wait();
+    allow_dependents();
+    __syncthreads();
     const float amax = scale_amax[1];
     const float s = block_scale<FMT>(amax);
-    const size_t n8 = n / 8;
-    const size_t stride = (size_t)gridDim.x * blockDim.x;
-    const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    auto encode8 = [&](const uint4& v, size_t i) {
-        float f[8], q[8];
-        unpack8(v, f);
-        block_quotients<1, 8>(f, s, q);
-        st_stream(codes + 8 * i, make_uint2(cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])));
-    };
-    size_t i = t0;
-    for (; i + stride < n8; i += 2 * stride) {     // two loads in flight per thread
-        const uint4 v0 = ld_stream(x + 8 * i);
-        const uint4 v1 = ld_stream(x + 8 * (i + stride));
-        encode8(v0, i);
-        encode8(v1, i + stride);
+    int si = 0;
+    bool ok = true;
+    for (; si < owned; ++si) {
+        const size_t t = t0 + si;
+        const bool staged = t < nstaged;
+        if (staged && !mbar_wait(&full[si], 0u)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* st = smem + (size_t)si * kTwStageBytes;
+#pragma unroll
+        for (int r = 0; r < kTwTile / (8 * kTwThreads); ++r) {
+            const unsigned e = r * 8 * kTwThreads + 8 * threadIdx.x;
+            const uint4 v = tw_load8(st, staged, x, n, t, e);
+            float f[8], q[8];
+            unpack8(v, f);
+            block_quotients<1, 8>(f, s, q);
+            const uint32_t w[2] = {cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]), cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7])};
+            const size_t g = t * kTwTile + e;
+            if (staged)
+                st_stream(codes + g, make_uint2(w[0], w[1]));
+            else
+                st_u8_tail(codes + g, w, 2, (long long)n - (long long)g);
+        }
     }
-    for (; i < n8; i += stride) encode8(ld_stream(x + 8 * i), i);
-    for (size_t i = 8 * n8 + t0; i < n; i += stride) {
-        float f[1] = {__uint_as_float((uint32_t)x[i] << 16)}, q[1];
-        block_quotients<1, 1>(f, s, q);
-        codes[i] = (uint8_t)cvt_fp8x2<FMT>(q[0], 0.0f);
+    if (__syncthreads_or(!ok)) {
+        if (threadIdx.x == 0) {
+            raise_error(kErrCopyTimeout);
+            for (int r = si; r < owned; ++r)
+                if (t0 + r < nstaged) mbar_wait(&full[r], 0u);
+        }
+        return;
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) scale_amax[0] = s;
 }
@@ -89,14 +177,18 @@ static fp8q_status_t launch_tensorwise(const uint16_t* x, size_t n, uint8_t* cod
     if (e != cudaSuccess) return cuda_status(e);
     static KernelCache kc1, kc2;
     int r1 = 0, r2 = 0;
-    fp8q_status_t pst = prepare_kernel(kc1, tensor_amax_kernel, 256, 0, 0, &r1);
-    if (pst == FP8Q_OK) pst = prepare_kernel(kc2, tensor_encode_kernel<FMT>, 256, 0, 0, &r2);
+    fp8q_status_t pst = prepare_kernel(kc1, tensor_amax_kernel, kTwThreads, kTwSmem, kTwSmem, &r1);
+    if (pst == FP8Q_OK) pst = prepare_kernel(kc2, tensor_encode_kernel<FMT>, kTwThreads, kTwSmem, kTwSmem, &r2);
     if (pst != FP8Q_OK) return pst;
-    const size_t units = (n + 7) / 8;
-    const fp8q_status_t st = launch(tensor_amax_kernel, grid_for((units + 255) / 256, r1), 256, 0, s, x, n, scale_amax);
+    const size_t tiles = (n + kTwTile - 1) / kTwTile;
+    const size_t grid = (tiles + kTwTilesPerCta - 1) / kTwTilesPerCta;
+    if (grid > 0x7FFFFFFFu) return FP8Q_ERR_SIZE;
+    const fp8q_status_t st = launch(tensor_amax_kernel, (unsigned)grid, kTwThreads, kTwSmem, s, x, n, scale_amax);
     if (st != FP8Q_OK) return st;
-    return launch(tensor_encode_kernel<FMT>, grid_for((units + 255) / 256, r2), 256, 0, s, x, n, codes, scale_amax);
+    return launch(tensor_encode_kernel<FMT>, (unsigned)grid, kTwThreads, kTwSmem, s, x, n, codes, scale_amax);
 }
+
+unsigned unit_errors_tensorwise(bool clear) { return read_unit_errors(clear); }
 
 }  // namespace fp8q
 
