@@ -761,6 +761,21 @@ def run_profile_case(case, launches):
     import torch
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if case == "ring_hop_256MiB":
+        # one e4m3 hop of the ring sweep's largest payload (2^27 elements,
+        # 256 MiB of bf16; outside the step), without the bf16 output
+        import gen
+        import weight_transfer_gb300 as w
+        n = (256 << 20) // 2
+        x0, x1 = gen.ring_partial(0, n).to(dev), gen.ring_partial(1, n).to(dev)
+        c0, s0 = w.fp8q_quantize_blockwise(x0, "e4m3")
+        c1, s1 = torch.empty_like(c0), torch.empty_like(s0)
+        for _ in range(max(1, launches)):
+            w.fp8q_ring_hop(c0, s0, x1, "e4m3", out_codes=c1, out_scales=s1)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": case, "kernel": "ring_hop_kernel", "launches": launches,
+                          "bytes_per_launch": bytes_hop(n, False)}))
+        return
     wl = Workload(dev, 0, torch)
     wl.run()                                   # every kernel's inputs exist
     torch.cuda.synchronize()
@@ -1378,7 +1393,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-vec3p5b", action="store_true", help="skip the 3.5e9-element vector row")
     ap.add_argument("--no-stack", action="store_true", help="skip the 48-layer MXFP8 stack row")
-    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES) + ["mxfp8_dequantize", "ring_allreduce_sim"],
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES) + ["mxfp8_dequantize", "ring_allreduce_sim", "ring_hop_256MiB"],
                     help="launch one kernel of the step a few times on its bench inputs and exit (for ncu)")
     ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()

@@ -28,8 +28,10 @@
 // A group of two or more hops (every rank's hop of one step of a simulated
 // ring) runs ring_hop_group_kernel: the same tiles and arithmetic, with the
 // per-tile bookkeeping hoisted out of the loop.  The kernel is bound by
-// instruction issue at large sizes (79% issue-active, 20 thread-instructions
-// per element on a 134M-element hop), so per-tile overhead shows directly.
+// instruction issue at large sizes (79% issue-active at 20.2
+// thread-instructions per element on a 134M-element hop with scalar
+// arithmetic; 71% at 16.6 with the packed arithmetic of hop_block16), so
+// per-element and per-tile instructions show directly in its time.
 #include "fp8q_device.cuh"
 #include "fp8q_host.cuh"
 
@@ -59,40 +61,107 @@ struct HopGroup {
     int64_t tile_start[kHopMaxGroup + 1];
     int count;
     int local_ready;       // the local partials may be read before the predecessor grid ends
+    float nzero;           // -0.0f
 };
+
+// Packed two-lane binary32 arithmetic (PTX f32x2: one instruction for two
+// values, each lane rounded exactly as the scalar instruction would round it),
+// the widening add of a bf16 and a binary32, and the three-input maximum.
+// They take the hop from about 20.5 to 17 thread-instructions per element.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// RN(bf16 + x): the bf16 widened exactly, then one rounded add.
+__device__ __forceinline__ float add_bf16_f32(uint16_t h, float x) {
+    float r;
+    asm("add.rn.f32.bf16 %0, %1, %2;" : "=f"(r) : "h"(h), "f"(x));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // One lane's share of one block: 16 incoming codes (ca, cb) with the block's
 // incoming scale s_in and 16 local bf16 values (la, lb) -> the fp32 sums y,
 // the block's new scale sc (amax over the 8 lanes of the block) and the 16
 // new codes (wa, wb).  REQ_BF16: requantize RNE_bf16(y), the bf16 partial a
 // receiver keeps, instead of the fp32 sum y (the alternative reading of the
-// hop).
+// hop).  nzero is -0.0f, passed in by the host.
+//
+// Every value is the one the scalar sequence gives, signed zeros included:
+//  * the product RN(d * s_in) is fma(d, s_in, -0): adding -0 to the exact
+//    product changes no value and no zero's sign, and as an fma there is no
+//    separate multiply left for the compiler to contract into the add (a
+//    packed multiply followed by an add was contracted, even with .rn);
+//  * y = RN(l + p) with l widened exactly, i.e. RN(p + l);
+//  * the quotient steps of markstein_div with -y formed exactly as y * -1
+//    and r * -RN(1/s) in place of -r * RN(1/s) (the same product).
 template <int FMT, bool REQ_BF16>
 __device__ __forceinline__ void hop_block16(const uint2& ca, const uint2& cb, const uint4& la, const uint4& lb,
-                                            float s_in, uint32_t (&wa)[2], uint32_t (&wb)[2], float (&y)[16],
-                                            float& sc) {
-    float d[16], lf[16];
+                                            float s_in, float nzero, uint32_t (&wa)[2], uint32_t (&wb)[2],
+                                            float (&y)[16], float& sc) {
+    float d[16];
     decode_fp8x4<FMT>(ca.x, d);
     decode_fp8x4<FMT>(ca.y, d + 4);
     decode_fp8x4<FMT>(cb.x, d + 8);
     decode_fp8x4<FMT>(cb.y, d + 12);
-    unpack8(la, *reinterpret_cast<float(*)[8]>(lf));
-    unpack8(lb, *reinterpret_cast<float(*)[8]>(lf + 8));
+    const uint32_t lw[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+    const uint64_t s2 = f2_pack(s_in, s_in), z2 = f2_pack(nzero, nzero);
     float a = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        y[i] = __fadd_rn(__fmul_rn(d[i], s_in), lf[i]);
-        if (REQ_BF16) y[i] = bf16_lo(pack_bf16x2(y[i], 0.0f));
-        a = fmaxf(a, fabsf(y[i]));
+    for (int i = 0; i < 8; ++i) {
+        float p0, p1;
+        f2_unpack(f2_fma(f2_pack(d[2 * i], d[2 * i + 1]), s2, z2), p0, p1);
+        y[2 * i] = add_bf16_f32((uint16_t)(lw[i] & 0xFFFFu), p0);
+        y[2 * i + 1] = add_bf16_f32((uint16_t)(lw[i] >> 16), p1);
+        if (REQ_BF16) {
+            y[2 * i] = bf16_lo(pack_bf16x2(y[2 * i], 0.0f));
+            y[2 * i + 1] = bf16_lo(pack_bf16x2(y[2 * i + 1], 0.0f));
+        }
+        a = max3(a, fabsf(y[2 * i]), fabsf(y[2 * i + 1]));
     }
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
     a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-    // a is a binary32 amax here, not a bf16 one: block_scale is exact for
-    // every binary32 dividend (its constant divisor makes that checkable)
     sc = block_scale<FMT>(a);
     float q[16];
-    block_quotients<2, 16>(y, sc, q);
+    if (sc >= 0x1p-58f) {
+        // block_quotients<2, 16> in packed form
+        const float yr = __frcp_rn(sc);
+        const uint64_t yr2 = f2_pack(yr, yr), nyr2 = f2_pack(-yr, -yr), sc2 = f2_pack(sc, sc);
+        const uint64_t m1 = f2_pack(-1.0f, -1.0f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint64_t y2 = f2_pack(y[2 * i], y[2 * i + 1]);
+            const uint64_t ny2 = f2_mul(y2, m1);
+            uint64_t q2 = f2_mul(y2, yr2);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint64_t r2 = f2_fma(q2, sc2, ny2);
+                q2 = f2_fma(r2, nyr2, q2);
+            }
+            f2_unpack(q2, q[2 * i], q[2 * i + 1]);
+        }
+    } else {
+        block_quotients<2, 16>(y, sc, q);      // s < 2^-58: the IEEE division
+    }
     wa[0] = cvt_fp8x4<FMT>(q[0], q[1], q[2], q[3]);
     wa[1] = cvt_fp8x4<FMT>(q[4], q[5], q[6], q[7]);
     wb[0] = cvt_fp8x4<FMT>(q[8], q[9], q[10], q[11]);
@@ -229,7 +298,7 @@ ring_hop_kernel(const __grid_constant__ HopGroup g) {
         uint32_t wa[2], wb[2];
         float y[16];
         float sc;
-        hop_block16<FMT, REQ_BF16>(ca, cb, la, lb, s_in, wa, wb, y, sc);
+        hop_block16<FMT, REQ_BF16>(ca, cb, la, lb, s_in, g.nzero, wa, wb, y, sc);
         uint8_t* out_codes = g.out_codes[h];
         uint16_t* out_bf16 = g.out_bf16[h];
         if (staged) {
@@ -291,6 +360,7 @@ struct HopGroupMulti {
     int64_t staged_end[kHopMaxGroup];          // global tiles below this one are staged (per hop)
     int count;
     int local_ready;
+    float nzero;
 };
 
 template <int FMT, bool REQ_BF16, int NST>
@@ -402,7 +472,7 @@ ring_hop_group_kernel(const __grid_constant__ HopGroupMulti g) {
         uint32_t wa[2], wb[2];
         float y[16];
         float sc;
-        hop_block16<FMT, REQ_BF16>(ca, cb, la, lb, s_in, wa, wb, y, sc);
+        hop_block16<FMT, REQ_BF16>(ca, cb, la, lb, s_in, g.nzero, wa, wb, y, sc);
         if (staged) {
             st_stream(out_codes + e, make_uint2(wa[0], wa[1]));
             st_stream(out_codes + e + 64, make_uint2(wb[0], wb[1]));
@@ -558,6 +628,7 @@ static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_
         g.tile_start[used] = start;
         g.count = used;
         g.local_ready = (flags & FP8Q_HOP_LOCAL_READY) ? 1 : 0;
+        g.nzero = -0.0f;
         const size_t tiles = (size_t)start;
         if (fmt == FP8Q_E4M3)
             return requant_bf16 ? launch_hop_group_kernel<kE4M3, true>(g, tiles, stream)
@@ -586,6 +657,7 @@ static fp8q_status_t launch_hops(const fp8q_hop_t* hops, int count, fp8q_format_
     g.tile_start[used] = start;
     g.count = used;
     g.local_ready = (flags & FP8Q_HOP_LOCAL_READY) ? 1 : 0;
+        g.nzero = -0.0f;
     const size_t tiles = (size_t)start;
     if (fmt == FP8Q_E4M3)
         return requant_bf16 ? launch_hop_kernel<kE4M3, true>(g, tiles, stream)
