@@ -143,3 +143,67 @@ def test_hop_signed_zeros_and_cancellation(w, orc, fmt, want_bf16):
     assert_same(u8(oc), ec, "codes")
     if want_bf16:
         assert_same(bits16(ob), eb, "bf16")
+
+
+def _near_boundary_blocks(orc, fmt, nblocks, seed):
+    """Incoming codes, scales and local partials for `nblocks` blocks in which
+    the quotients y / s (y the fp32 sums, s the block's new scale) lie within
+    a few binary32 ulps of FP8 rounding boundaries, where a quotient one ulp
+    off changes the code.  Element 0 of a block is a zero code with a bf16
+    local A, which fixes the amax, so s = RN(A / Fmax).  The incoming scale is
+    then s_in = RN(m * s / d) for a random code value d and a random midpoint
+    m between two adjacent FP8 values: every code d * 2^j (either sign) of a
+    lane decodes to a product within an ulp or two of m * 2^j * s, and the
+    lane's local adds k ulps of that product (|k| <= 3, exact in bf16)."""
+    rng = np.random.default_rng(seed)
+    F = 448.0 if fmt == 0 else 57344.0
+    min_normal = 2.0 ** (-6 if fmt == 0 else -14)
+    vals = orc.decode(fmt, np.arange(0x80, dtype=np.uint8)).astype(np.float64)   # the positive codes, ascending
+    fin = np.isfinite(vals)
+    codes, scales, local = [], [], []
+    for _ in range(nblocks):
+        A = float(orc.bf16_to_f32(orc.f32_to_bf16(np.float32(rng.uniform(1, 2) * 2.0 ** int(rng.integers(-8, 8)))))[0])
+        s = np.float32(np.float32(A) / np.float32(F))
+        # a midpoint m between adjacent normal values below F / 4, a normal code value d
+        lo_i = int(rng.choice(np.nonzero(fin & (vals >= min_normal) & (vals < F / 4))[0]))
+        m = (vals[lo_i] + vals[lo_i + 1]) / 2
+        d_i = int(rng.choice(np.nonzero(fin & (vals >= min_normal) & (vals <= F / 2))[0]))
+        d = vals[d_i]
+        s_in = np.float32(m * float(s) / d)
+        # the lanes' codes: d * 2^j with m * 2^j in [min_normal, F / 2] and d * 2^j a normal code
+        cand = [c for c in range(1, 0x7F) if fin[c] and vals[c] >= min_normal and
+                (vals[c] / d) == 2.0 ** np.round(np.log2(vals[c] / d)) and
+                min_normal <= m * vals[c] / d <= F / 2]
+        assert cand
+        lanes = rng.choice(cand, 127) | (rng.integers(0, 2, 127) << 7)
+        p = (orc.decode(fmt, lanes.astype(np.uint8)) * s_in).astype(np.float32)
+        ulp = np.spacing(np.abs(p)).astype(np.float32)
+        k = rng.integers(-3, 4, 127).astype(np.float32)
+        lb = orc.f32_to_bf16((k * ulp).astype(np.float32))
+        assert np.array_equal(orc.bf16_to_f32(lb), (k * ulp).astype(np.float32))     # exact in bf16
+        codes.append(np.concatenate([[0], lanes]).astype(np.uint8))
+        local.append(np.concatenate([orc.f32_to_bf16(np.float32(A)), lb]).astype(np.uint16))
+        scales.append(s_in)
+    return np.concatenate(codes), np.array(scales, np.float32), np.concatenate(local)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_hop_quotients_near_fp8_boundaries(w, orc, fmt):
+    # the hop's quotient y / s in the two-step reciprocal form must equal the
+    # IEEE quotient wherever it decides a code: 48 staged blocks and a ragged
+    # partial block, through the single-hop kernel and a group of two hops
+    codes, scales, lb = _near_boundary_blocks(orc, fmt, 49, seed=77 + fmt)
+    n = 48 * 128 + 77
+    codes, lb = codes[:n], lb[:n]
+    ec, es, eb = orc.ring_hop(codes, scales, lb, fmt)
+    dc, ds, dl = torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(), bf16_from_bits(lb)
+    oc, os_, ob = w.fp8q_ring_hop(dc, ds, dl, fmt, want_bf16=True)
+    assert_same_f32(os_.cpu().numpy(), es, "scales")
+    assert_same(u8(oc), ec, "codes")
+    assert_same(bits16(ob), eb, "bf16")
+    outs = w.fp8q_ring_hop_group([{"in_codes": dc, "in_scales": ds, "local": dl},
+                                  {"in_codes": dc, "in_scales": ds, "local": dl, "want_bf16": True}], fmt)
+    for gc, gs, gb in outs:
+        assert_same_f32(gs.cpu().numpy(), es, "group scales")
+        assert_same(u8(gc), ec, "group codes")
+    assert_same(bits16(outs[1][2]), eb, "group bf16")
