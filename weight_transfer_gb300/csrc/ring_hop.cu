@@ -9,8 +9,8 @@
 // is reduced, nothing is re-read from HBM.
 //
 // Work split: a persistent CTA of 256 threads walks tiles of 32 blocks
-// (4096 elements).  Thread 0 keeps up to 3 tiles in flight (2 on short
-// hops, see launch_hop_kernel); a tile
+// (4096 elements).  Thread 0 keeps up to 3 tiles in flight (2 in short hop
+// groups, see launch_hop_group_kernel); a tile
 // is three bulk copies into one shared-memory stage (4096 incoming codes,
 // their 32 scales, 8 KB of the local bf16 partial) armed on the stage's
 // mbarrier.  Once it has landed, 8 lanes own one block: lane j takes
@@ -545,7 +545,9 @@ static fp8q_status_t launch_hop_group_kernel_n(const HopGroupMulti& g, size_t ti
     return launch(ring_hop_group_kernel<FMT, REQ, NST>, grid_for(tiles, resident), kHopThreads, smem, stream, g);
 }
 
-// The stage count as for single hops (see launch_hop_kernel).
+// A short group (under 8 tiles per CTA of a full grid) runs 2 stages, a long
+// one 3: the 8-rank AllReduce of the 8 x 13.1M bucket, whose hop groups are
+// 3,200 tiles each, takes 119.0 us with 2 stages and 120.0 with 3.
 template <int FMT, bool REQ>
 static fp8q_status_t launch_hop_group_kernel(const HopGroupMulti& g, size_t tiles, cudaStream_t stream) {
     if (tiles < (size_t)8 * 4 * (size_t)sm_count()) return launch_hop_group_kernel_n<FMT, REQ, 2>(g, tiles, stream);
@@ -562,14 +564,14 @@ static fp8q_status_t launch_hop_kernel_n(const HopGroup& g, size_t tiles, cudaSt
     return launch(ring_hop_kernel<FMT, REQ, NST>, grid_for(tiles, resident), kHopThreads, smem, stream, g);
 }
 
-// A short hop (under 8 tiles per CTA of a full persistent grid, e.g. the
-// 13.1M-element shard: 3,200 tiles over 608 CTAs) is ramp-up and tail, and
-// 2 stages start it sooner (the 7-hop chain at 13.1M: 75.0 against 77.0 us);
-// a long one needs the third stage's bytes in flight (64 MiB per hop: 170.5
-// against 173.0 us).
+// Single hops run 3 stages at every size.  With scalar arithmetic a short hop
+// (under 8 tiles per CTA of a full grid, e.g. the 13.1M-element shard: 3,200
+// tiles over 608 CTAs) was faster with 2 (the 7-hop chain at 13.1M: 75.0
+// against 77.0 us); with the packed arithmetic of hop_block16 the third stage
+// pays there too (the chain 75.7 -> 73.3 us, and 2 stages lose 5 us at
+// 64 MiB per hop).
 template <int FMT, bool REQ>
 static fp8q_status_t launch_hop_kernel(const HopGroup& g, size_t tiles, cudaStream_t stream) {
-    if (tiles < (size_t)8 * 4 * (size_t)sm_count()) return launch_hop_kernel_n<FMT, REQ, 2>(g, tiles, stream);
     return launch_hop_kernel_n<FMT, REQ, 3>(g, tiles, stream);
 }
 
