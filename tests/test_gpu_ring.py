@@ -81,14 +81,15 @@ def test_ring_chain_full_check(w, orc, fmt, payload):
     assert_same(bits16(last), b, "final bf16")
 
 
-@pytest.mark.parametrize("payload", [1 << 25, 1 << 26, 1 << 27, 1 << 28])
-def test_ring_chain_large_sampled(w, orc, payload):
+@pytest.mark.parametrize("fmt,payload", [(0, 1 << 25), (0, 1 << 26), (0, 1 << 27), (0, 1 << 28), (1, 1 << 26),
+                                         (1, 1 << 28)])
+def test_ring_chain_large_sampled(w, orc, fmt, payload):
     # 32 MiB .. 256 MiB per-hop payloads, checked on sampled 128-blocks:
     # every hop is block-local, so the oracle replays the chain of a block
     # from that block's slice of the 8 partials
     n = payload // 2
     host = [gen.ring_partial(r, n) for r in range(gen.RING_PARTIALS)]
-    hops, last = run_chain_gpu(w, [p.cuda() for p in host], 0)
+    hops, last = run_chain_gpu(w, [p.cuda() for p in host], fmt)
     nb = n // 128
     rng = np.random.default_rng(payload >> 20)
     blocks = np.unique(np.concatenate([rng.integers(0, nb, 400), [0, nb - 1]]))
@@ -98,11 +99,11 @@ def test_ring_chain_large_sampled(w, orc, payload):
     gpu_last = bits16(last)
     for b in blocks:
         sl = slice(128 * b, 128 * b + 128)
-        c, s = orc.quantize_blockwise(hb[0][sl].copy(), 0)
+        c, s = orc.quantize_blockwise(hb[0][sl].copy(), fmt)
         for h in range(1, gen.RING_PARTIALS):
             assert_same(gpu_codes[h - 1][sl], c, f"block {b} hop {h - 1}")
             assert gpu_scales[h - 1][b] == s[0]
-            c, s, bf = orc.ring_hop(c, s, hb[h][sl].copy(), 0)
+            c, s, bf = orc.ring_hop(c, s, hb[h][sl].copy(), fmt)
         assert_same(gpu_codes[-1][sl], c, f"block {b} final")
         assert_same(gpu_last[sl], bf, f"block {b} bf16")
 
