@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import math
 import hashlib
 import json
 import os
@@ -252,6 +253,23 @@ class L2Flush:
 
 
 # ------------------------------------------------------------ workload ----
+def carve(torch, specs, device=None, pin=False):
+    """One uint8 allocation holding a tensor of each (shape, dtype) in
+    `specs`, at 256-byte aligned offsets (on `device`, or in pinned host
+    memory with pin=True).  Returns (buffer, [tensors])."""
+    offs, total = [], 0
+    for shape, dt in specs:
+        nbytes = math.prod(shape) * torch.empty(0, dtype=dt).element_size()
+        offs.append((total, nbytes))
+        total += (nbytes + 255) // 256 * 256
+    if device is None:
+        buf = torch.empty(total, dtype=torch.uint8, pin_memory=pin)
+    else:
+        buf = torch.empty(total, dtype=torch.uint8, device=device)
+    views = [buf[o:o + nb].view(dt).view(shape) for (o, nb), (shape, dt) in zip(offs, specs)]
+    return buf, views
+
+
 class DeviceSet:
     """One set of device buffers for a step (inputs and outputs) and the
     step's launch list bound to them, arguments marshalled once so that a
@@ -262,23 +280,21 @@ class DeviceSet:
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         nb = nscales(n)
         self.stream = stream
-        self.bucket = torch.empty((k, n), dtype=bf, device=dev)
-        self.layer = [torch.empty(h.shape, dtype=bf, device=dev) for h in wl.h_layer]
-        self.q = {f: (torch.empty((k, n), dtype=u8, device=dev), torch.empty((k, nb), dtype=f32, device=dev))
-                  for f in (0, 1)}
-        self.red = {f: (torch.empty(n, dtype=bf, device=dev), torch.empty(n, dtype=f32, device=dev)) for f in (0, 1)}
+        # the step's inputs in one allocation and the results a caller reads
+        # back in another, each a run of tensors (wl.in_specs, wl.out_specs),
+        # so that each direction of the end-to-end run is one copy
+        self.in_buf, ins = carve(torch, wl.in_specs, dev)
+        self.bucket, self.layer = ins[0], ins[1:]
+        self.out_buf, outs = carve(torch, wl.out_specs, dev)
+        self.q = {0: (outs[0], outs[1]), 1: (outs[2], outs[3])}
+        self.red = {0: (outs[4], outs[5]), 1: (outs[6], outs[7])}
+        # hops 1..6 are internal; the last hop's codes and scales are results
         self.hops = [(torch.empty(n, dtype=u8, device=dev), torch.empty(nb, dtype=f32, device=dev))
-                     for _ in range(k - 1)]
-        self.ring_bf16 = torch.empty(n, dtype=bf, device=dev)
-        self.mx = []
-        for (name, b, m, kk) in wl.tensors:
-            sb = wl.w.mxfp8_swizzled_scale_bytes(b, m, kk)
-            self.mx.append((torch.empty((b, m, kk), dtype=u8, device=dev), torch.empty(sb, dtype=u8, device=dev), sb))
-        # the results a caller reads back
-        self.outputs = [self.q[0][0], self.q[0][1], self.q[1][0], self.q[1][1], self.red[0][0], self.red[0][1],
-                        self.red[1][0], self.red[1][1], self.hops[-1][0], self.hops[-1][1], self.ring_bf16]
-        for c, sc, _ in self.mx:
-            self.outputs += [c, sc]
+                     for _ in range(k - 2)] + [(outs[8], outs[9])]
+        self.ring_bf16 = outs[10]
+        self.mx = [(outs[11 + 2 * i], outs[12 + 2 * i], wl.w.mxfp8_swizzled_scale_bytes(b, m, kk))
+                   for i, (name, b, m, kk) in enumerate(wl.tensors)]
+        self.outputs = outs
 
         vp = ctypes.c_void_p
         sp_ = vp(stream.cuda_stream)
@@ -386,6 +402,17 @@ class Workload:
         self.h_bucket = host
         self.tensors = gen.QWEN3_TENSORS
         self.h_layer = [gen.qwen3_tensor(rank, t).pin_memory() for t in range(len(self.tensors))]
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        nb = nscales(n)
+        self.in_specs = [((k, n), bf)] + [(tuple(h.shape), bf) for h in self.h_layer]
+        self.out_specs = [((k, n), u8), ((k, nb), f32), ((k, n), u8), ((k, nb), f32), ((n,), bf), ((n,), f32),
+                          ((n,), bf), ((n,), f32), ((n,), u8), ((nb,), f32), ((n,), bf)]
+        for (name, b, m, kk) in self.tensors:
+            self.out_specs += [((b, m, kk), u8), ((w.mxfp8_swizzled_scale_bytes(b, m, kk),), u8)]
+        # the inputs in pinned host memory, laid out as a device set's inputs
+        self.h_in, hv = carve(torch, self.in_specs, pin=True)
+        for dst, src in zip(hv, [host] + self.h_layer):
+            dst.copy_(src)
         self.stream = torch.cuda.current_stream(dev)
         self.sets = [DeviceSet(self, self.stream)]
         self.h2d(self.sets[0], self.stream)
@@ -409,11 +436,12 @@ class Workload:
 
     def _copy_all(self, stream, pairs):
         """Copies (dst, src) tensor pairs on `stream`, one cudaMemcpyAsync per
-        tensor.  On this GPU's host link one copy per tensor is the fastest
-        form: fanning each direction out over 4 side streams in 32 MiB pieces
-        gave 370 GB/s end to end against 386 GB/s (the link itself carries
-        about 210 GB/s host to device, 190 GB/s back, and 310-340 GB/s both
-        ways at once, by copy engine or SM alike)."""
+        pair.  Each direction of a step is one pair (the inputs and the
+        results each lie in one buffer).  Fanning a direction out over 4 side
+        streams in 32 MiB pieces gave 370 GB/s end to end, one copy per tensor
+        386 GB/s, one copy per direction 388 GB/s; the host link carries
+        about 210 GB/s host to device and 190 GB/s back, by copy engine or SM
+        alike."""
         torch = self.torch
         nbytes = 0
         with torch.cuda.stream(stream):
@@ -424,13 +452,13 @@ class Workload:
 
     def h2d(self, ds, stream):
         """Copies the step's inputs from pinned host memory into set `ds`."""
-        return self._copy_all(stream, [(ds.bucket, self.h_bucket)] + list(zip(ds.layer, self.h_layer)))
+        return self._copy_all(stream, [(ds.in_buf, self.h_in)])
 
     def d2h(self, ds, stream):
         """Reads every result of set `ds` back into pinned host memory."""
         if self.h_out is None:
-            self.h_out = [self.torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in ds.outputs]
-        return self._copy_all(stream, list(zip(self.h_out, ds.outputs)))
+            self.h_out_buf, self.h_out = carve(self.torch, self.out_specs, pin=True)
+        return self._copy_all(stream, [(self.h_out_buf, ds.out_buf)])
 
     def e2e(self, steps, warmup=2):
         """Steady-state end-to-end throughput of the public API with host
@@ -1583,8 +1611,8 @@ def main():
                 "copy_GBps_alone": getattr(wl, "copy_gbps", None),
                 "outputs_equal_device_run": getattr(wl, "e2e_outputs_equal", None),
                 "host": topo,
-                "pipeline": "H2D, kernels and D2H on three streams (one cudaMemcpyAsync per tensor), two device "
-                            "buffer sets"},
+                "pipeline": "H2D, kernels and D2H on three streams (one cudaMemcpyAsync per direction: the "
+                            "inputs and the results each lie in one buffer), two device buffer sets"},
         "gpu_launches": nl * steps,
         "fused_vs_naive_reduce": fvn,
         "next_rows": extras,
