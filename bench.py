@@ -1540,8 +1540,14 @@ def main():
     value_gbs = bytes_all / (ms_step * 1e-3) / 1e9
 
     # ---------------- end to end: host buffers through the C ABI -----------
+    # three windows, the median reported: the host link is shared with the
+    # machine's other GPUs, and one window can land on a neighbour's transfer
     barrier()
-    e2e_local, bi, bo = wl.e2e(max(1, min(args.e2e_steps, steps)))
+    e2e_windows = []
+    for _ in range(3):
+        ms_w, bi, bo = wl.e2e(max(1, min(args.e2e_steps, steps)))
+        e2e_windows.append(ms_w)
+    e2e_local = sorted(e2e_windows)[1]
     barrier()
     clocks.stop()
     e2e_ms, _, _ = combine_over_ranks(dist if world > 1 else None, dev, e2e_local, 0.0, 0.0)
@@ -1608,6 +1614,8 @@ def main():
                            "what": "programmatic dependent launch of every kernel (on in the timed steps)"},
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps,
+                "windows_ms_per_step": [round(x, 3) for x in e2e_windows],
+                "what": f"median of 3 windows of {e2e_steps} pipelined steps",
                 "copy_GBps_alone": getattr(wl, "copy_gbps", None),
                 "outputs_equal_device_run": getattr(wl, "e2e_outputs_equal", None),
                 "host": topo,
