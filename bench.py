@@ -395,24 +395,21 @@ class Workload:
         self.L = w.lib()
         n, k = gen.DDP_N, gen.DDP_K
         self.n, self.k = n, k
-        # the bucket of all 8 ranks in one allocation: shard r = rows r
-        host = torch.empty((k, n), dtype=torch.bfloat16, pin_memory=True)
-        for r, seed in enumerate(rank_data_seeds(rank, k)):
-            host[r].copy_(gen.ddp_shard(seed))
-        self.h_bucket = host
         self.tensors = gen.QWEN3_TENSORS
-        self.h_layer = [gen.qwen3_tensor(rank, t).pin_memory() for t in range(len(self.tensors))]
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         nb = nscales(n)
-        self.in_specs = [((k, n), bf)] + [(tuple(h.shape), bf) for h in self.h_layer]
+        # inputs: the bucket of all 8 ranks (shard r = row r), then the layer's tensors
+        self.in_specs = [((k, n), bf)] + [((b, m, kk), bf) for (name, b, m, kk) in self.tensors]
         self.out_specs = [((k, n), u8), ((k, nb), f32), ((k, n), u8), ((k, nb), f32), ((n,), bf), ((n,), f32),
                           ((n,), bf), ((n,), f32), ((n,), u8), ((nb,), f32), ((n,), bf)]
         for (name, b, m, kk) in self.tensors:
             self.out_specs += [((b, m, kk), u8), ((w.mxfp8_swizzled_scale_bytes(b, m, kk),), u8)]
         # the inputs in pinned host memory, laid out as a device set's inputs
         self.h_in, hv = carve(torch, self.in_specs, pin=True)
-        for dst, src in zip(hv, [host] + self.h_layer):
-            dst.copy_(src)
+        for r, seed in enumerate(rank_data_seeds(rank, k)):
+            hv[0][r].copy_(gen.ddp_shard(seed))
+        for t in range(len(self.tensors)):
+            hv[1 + t].copy_(gen.qwen3_tensor(rank, t))
         self.stream = torch.cuda.current_stream(dev)
         self.sets = [DeviceSet(self, self.stream)]
         self.h2d(self.sets[0], self.stream)
